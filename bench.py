@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Throughput of paged-attention decode on one GB300 (one JSON line on stdout).
+
+Workload: batched paged decode in bf16 -- 64 sequences with lengths drawn
+U[512, 4096], 32 query heads over 8 KV heads, head_dim 128, 16-token pages
+placed by a random permutation of the block pool (seeded, synthetic).  One
+step is one pass of the whole decode path over the batch: the split-KV
+partial kernel (block-table walk, paged K/V gather, QK^T, online softmax,
+PV) and the log-sum-exp merge.  The KV cache (604 MB) is larger than L2, and
+L2 is additionally flushed (a 2x-L2 write) between timed steps, outside the
+timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``value`` is decode KV GB/s: the algorithmic bytes of a step (every cached
+token's K and V row for its KV head, the queries, outputs, block-table
+entries and lengths; partials are overhead and not counted) divided by the
+step's device time.  ``--impl reference`` times the float64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+import os
+
+# The oracle legs run single-threaded: say so and make it so (before numpy loads BLAS).
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% of HBM peak) and tokens/s; prefill TFLOP/s, 1 GB300"
+WORKLOAD = ("batched paged decode, bf16 KV: 64 seqs, seq_lens U[512,4096], 32 q / 8 kv heads, head_dim 128, "
+            "block_size 16, block_table a random permutation of the pool")
+PARTITION = 512
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def decode_algorithmic_bytes(case) -> int:
+    """K and V rows of every cached token (per KV head) + q + out + block-table entries + lengths."""
+    esize = case.k_cache.element_size()
+    lens = case.seq_lens.numpy().astype(np.int64)
+    kv = int(lens.sum()) * case.G * case.D * 2 * esize
+    qo = 2 * case.S * case.H * case.D * case.q.element_size()
+    table = int(sum(-(-int(L) // case.bs) for L in lens)) * 4 + 4 * case.S
+    return kv + qo + table
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_attention_kv_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "decode_bf16_kernel_batched_decode.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples (100 ms) while the GPU works."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.rows.append((time.time(), parts))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = [p for _, p in self.rows if not self.uuid or self.uuid in p[1]] or [p for _, p in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable: no nvidia-smi samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in rows if num(p[2]) is not None]
+        smax = [num(p[3]) for p in rows if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in rows for i in range(4) if p[6 + i].lower() == "active"})
+        busy = [x for x in sm if smax and x > 0.5 * max(smax)] or sm
+        return {"sm_mhz": float(np.median(busy)) if busy else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(p[4]) or 0.0) for p in rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+def oracle_step(case, seqs):
+    import oracle
+    oracle.paged_decode(case.q[seqs], case.k_cache, case.v_cache, case.block_table[seqs], case.seq_lens[seqs],
+                        case.scale)
+
+
+def sub_bytes(case, seqs) -> int:
+    from paged_attention_kv_decode_gb300 import workloads as wl
+    sub = wl.DecodeCase(name="sample", q=case.q[seqs], k_cache=case.k_cache, v_cache=case.v_cache,
+                        block_table=case.block_table[seqs], seq_lens=case.seq_lens[seqs], scale=case.scale)
+    return decode_algorithmic_bytes(sub)
+
+
+def cpu_baseline(case, budget_s=10.0):
+    """The oracle, as it stands, on the whole batch repeated until ~budget_s of CPU work."""
+    seqs = np.arange(case.S)
+    nbytes = decode_algorithmic_bytes(case)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_step(case, seqs)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the full 64-sequence batch, {reps} pass(es), float64 NumPy, {dt:.1f} s wall"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from paged_attention_kv_decode_gb300 import workloads as wl
+    case = wl.config2_batched_decode()
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    oracle_step(case, np.arange(1))
+    per_seq = max(time.perf_counter() - t0, 1e-3)
+    budget = 150.0
+    n = int(max(1, min(case.S, budget / max(1, args.steps + args.warmup) / per_seq)))
+    samples = [rng.choice(case.S, size=n, replace=False) for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        oracle_step(case, samples[i])
+    tot_bytes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = samples[args.warmup + i]
+        oracle_step(case, s)
+        tot_bytes += sub_bytes(case, s)
+    dt = time.perf_counter() - t0
+    value = tot_bytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_seqs_per_step": n},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} of 64 sequences per step (random), float64 NumPy"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import paged_attention_kv_decode_gb300 as pa
+    from paged_attention_kv_decode_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = wl.config2_batched_decode()
+    P = args.partition
+    S, H, D = case.S, case.H, case.D
+    max_len = case.max_seq_len
+    q = case.q.to(dev)
+    kc = case.k_cache.to(dev)
+    vc = case.v_cache.to(dev)
+    bt = case.block_table.to(dev)
+    sl = case.seq_lens.to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, pa.metis_decode_workspace_bytes(S, H, D, max_len, P)), dtype=torch.uint8, device=dev)
+    part_out, part_lse = pa.split_workspace_views(ws, S, H, D, max_len, P)
+    nbytes = decode_algorithmic_bytes(case)
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(max(2 * int(getattr(props, "L2_cache_size", 128 << 20)), 256 << 20), dtype=torch.uint8,
+                        device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.metis_paged_attn_decode_partials(q, kc, vc, bt, sl, case.scale, partition_size=P, max_seq_len=max_len,
+                                            workspace=ws, stream=stream)
+        ev_mid.record(stream)
+        pa.metis_merge_attn_states(part_out, part_lse, sl, P, out=out, stream=stream)
+
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    # clock ramp (untimed), then W warm-up steps
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pa.metis_read_status(clear=True)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark()
+    for i in range(args.steps):
+        flush.zero_()                      # untimed: evict L2 between steps
+        starts[i].record(stream)
+        ev_mid = mids[i]
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.mark()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kern_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+    status = pa.metis_read_status(clear=True)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    kern_avg_ms = float(np.mean(kern_ms))
+    merge_avg_ms = float(np.mean([a - b for a, b in zip(step_ms, kern_ms)]))
+
+    # end to end through the public call: pinned host inputs -> device, decode, output -> pinned host
+    h_q = case.q.pin_memory()
+    h_bt = case.block_table.pin_memory()
+    h_sl = case.seq_lens.pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d_q, d_bt, d_sl = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
+    e2e_n = args.steps
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_n)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_n)]
+
+    def e2e_step(i):
+        e_s[i].record(stream)
+        d_q.copy_(h_q, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        pa.metis_paged_attn_decode(d_q, kc, vc, d_bt, d_sl, case.scale, out=out, partition_size=P,
+                                   max_seq_len=max_len, workspace=ws, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        e_e[i].record(stream)
+
+    for i in range(min(3, e2e_n)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(e2e_n):
+        flush.zero_()
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.stop()
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), world, dev)
+    h2d = h_q.numel() * h_q.element_size() + h_bt.numel() * 4 + h_sl.numel() * 4
+    d2h = h_out.numel() * h_out.element_size()
+
+    if rank != 0:
+        return 0
+    peak, peak_src = load_peaks()
+    achieved = nbytes / (kern_avg_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "partition_size": P, "tokens": int(case.seq_lens.sum()),
+                   "kv_bytes_per_step": nbytes, "l2": "inputs larger than L2 (KV 604 MB) and L2 flushed "
+                                                      "between timed steps (untimed 2x-L2 write)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": world * S * args.steps / (total_ms * 1e-3),
+        "hbm_frac": value / peak,
+        "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel", "achieved": achieved, "peak": peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic(), "kernel_ms": kern_avg_ms, "merge_ms": merge_avg_ms,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "e2e": {"value": world * nbytes * e2e_n / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_n,
+                "note": "KV cache resident in HBM; per step: q, block table, lengths H2D from pinned memory, "
+                        "output D2H to pinned memory"},
+        "gpu_launches": 2 * args.steps,
+        "device_status": status,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition", type=int, default=PARTITION)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3 (the minimum)")
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    else:
+        rc = run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,175 @@
+/*
+ * metis_attn -- attention over a paged KV cache on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one the vLLM plugin pages build on: paged attention
+ * and MLA kernels fed by the scheduler's block tables and sequence lengths
+ * (vllm-metal architecture article, sections 3 and 4), with prefix caching and
+ * chunked prefill on the engine side (vllm-metis 0.1.0 page, introduction and
+ * "How the model maps onto vLLM", "Caches").  The pages name the operation but
+ * print no formula; every entry point computes textbook scaled-dot-product
+ * softmax attention of each query row over the tokens its sequence has cached:
+ *
+ *     z_t = scale * q . k_t,   out = sum_t softmax(z)_t v_t,   lse = ln sum_t exp(z_t)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *   library never allocates, frees, copies to or from the host, or
+ *   synchronises inside a compute call, so calls can be captured in a CUDA
+ *   graph.  Tensors are dense, row-major (C order), 16-byte aligned.
+ * Stream.  `stream` is a cudaStream_t passed as void*; NULL is the legacy
+ *   default stream.  Work is enqueued asynchronously on it.
+ * KV pages.  k_cache / v_cache are [num_blocks, block_size, num_kv_heads,
+ *   head_dim].  Logical token t of sequence s is in physical block
+ *   block_table[s * max_blocks + t / block_size], slot t % block_size.
+ *   block_table is int32 [num_seqs, max_blocks]; only its first
+ *   ceil(seq_lens[s] / block_size) entries of row s are read.  seq_lens is
+ *   int32 [num_seqs]: the number of cached tokens, INCLUDING the queried ones
+ *   (their K/V must already be in the pages).  Page slots at or beyond
+ *   seq_lens[s] are never used, so they may hold anything (NaN included).
+ * GQA.  q head h reads kv head h / (num_heads / num_kv_heads).
+ * dtype.  METIS_F32 or METIS_BF16; q, the caches and out share it.  All
+ *   accumulation, the softmax statistics, lse and split partials are fp32.
+ * lse.  Natural-log log-sum-exp of the scaled scores, fp32; -inf for an
+ *   empty sequence (whose output row is 0).
+ * Errors.  Return 0 on success.  A negative METIS_E_* code means the
+ *   arguments were rejected on the host and NOTHING was launched;
+ *   metis_last_error() then holds a message.  METIS_E_CUDA means a launch
+ *   failed.  Content errors that only the device can see (a block id outside
+ *   [0, num_blocks), a sequence longer than its table row or than
+ *   max_seq_len) never fault: the offending page reads as zeros, and a bit
+ *   is set in the device status word read by metis_read_status().
+ */
+#ifndef METIS_ATTN_H
+#define METIS_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtypes */
+#define METIS_F32  0
+#define METIS_BF16 1
+
+/* status codes */
+#define METIS_OK              0
+#define METIS_E_NULL         -1  /* a required pointer is NULL */
+#define METIS_E_SHAPE        -2  /* inconsistent or non-positive sizes */
+#define METIS_E_UNSUPPORTED  -3  /* head_dim / block_size / head ratio / dtype not built */
+#define METIS_E_ALIGN        -4  /* a pointer is not 16-byte aligned */
+#define METIS_E_WORKSPACE    -5  /* workspace NULL or smaller than required */
+#define METIS_E_CUDA         -6  /* a CUDA call failed (message in metis_last_error) */
+
+/* device status word bits (metis_read_status) */
+#define METIS_STATUS_BAD_BLOCK_ID  1u  /* a block id outside [0, num_blocks) */
+#define METIS_STATUS_SEQ_TOO_LONG  2u  /* seq_lens[s] > max_blocks * block_size or > max_seq_len */
+#define METIS_STATUS_WAIT_TIMEOUT  4u  /* a pipeline wait gave up (a library bug) */
+#define METIS_STATUS_BAD_Q_LEN     8u  /* prefill: q_len > seq_len or a negative q_len */
+
+/*
+ * metis_paged_attn_decode -- one query token per sequence over its pages
+ * (the paged-attention kernel of the vllm-metal article, section 3, fed by
+ * the block table and sequence lengths of section 4).
+ *
+ *   q            [num_seqs, num_heads, head_dim]      dtype
+ *   k_cache      [num_blocks, block_size, num_kv_heads, head_dim]
+ *   v_cache      same shape as k_cache
+ *   block_table  int32 [num_seqs, max_blocks]
+ *   seq_lens     int32 [num_seqs]; the query is the last cached token
+ *   out          [num_seqs, num_heads, head_dim]      dtype (written)
+ *   lse_out      fp32 [num_seqs, num_heads] or NULL   (written when non-NULL)
+ *   scale        softmax scale (e.g. 1/sqrt(head_dim))
+ *   partition_size
+ *                0: one pass over each sequence.  > 0: split-KV -- tokens
+ *                [p*P, (p+1)*P) form partition p; each partition's normalised
+ *                partial output and lse go to the workspace, then
+ *                metis_merge_attn_states' kernel combines them on the same
+ *                stream.  Must be a positive multiple of 16.
+ *   max_seq_len  host-side upper bound on seq_lens (sizes the grid); tokens
+ *                beyond it are not read (status bit SEQ_TOO_LONG).
+ *   workspace    device scratch of at least metis_decode_workspace_bytes(...)
+ *                bytes (may be NULL when that is 0); contents need no
+ *                initialisation and are clobbered.
+ *
+ * Supported: head_dim in {64, 128}; block_size in {16, 32, 64}; bf16 needs
+ * num_heads / num_kv_heads in {1, 2, 4, 8}; fp32 any ratio up to 8.
+ * num_seqs == 0 is a successful no-op.
+ */
+int metis_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            void* out, float* lse_out,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks, int num_blocks, int dtype,
+                            float scale, int partition_size, int max_seq_len,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * metis_paged_attn_decode_partials -- the first half of a split-KV decode:
+ * the same arguments as metis_paged_attn_decode without out / lse_out, and
+ * partition_size must be > 0.  Writes each partition's normalised partial
+ * output and lse into the workspace and launches nothing else; the second
+ * half is metis_merge_attn_states over
+ *
+ *   part_out = (float*)workspace                       [num_seqs, num_heads, max_parts, head_dim]
+ *   part_lse = (float*)((char*)workspace + align256(4 * num_seqs * num_heads * max_parts * head_dim))
+ *                                                       [num_seqs, num_heads, max_parts]
+ *
+ * with max_parts = ceil(max_seq_len / partition_size).  Partitions past a
+ * sequence's end are not written (the merge does not read them).
+ */
+int metis_paged_attn_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_blocks, int num_blocks, int dtype,
+                                     float scale, int partition_size, int max_seq_len,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace metis_paged_attn_decode needs (0 when partition_size == 0). */
+size_t metis_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                    int max_seq_len, int partition_size);
+
+/*
+ * metis_merge_attn_states -- the log-sum-exp merge of split-KV partials:
+ *
+ *   lse = m + ln sum_p exp(lse_p - m),  m = max_p lse_p
+ *   out = sum_p exp(lse_p - lse) * o_p
+ *
+ * over partitions p < min(ceil(seq_lens[s] / partition_size), max_parts);
+ * partitions with lse_p = -inf weigh nothing, and a sequence with no
+ * partition gets out = 0, lse = -inf.
+ *
+ *   part_out   fp32 [num_seqs, num_heads, max_parts, head_dim] (normalised o_p)
+ *   part_lse   fp32 [num_seqs, num_heads, max_parts]            (natural log)
+ *   seq_lens   int32 [num_seqs]
+ *   out        [num_seqs, num_heads, head_dim] in out_dtype (written)
+ *   lse_out    fp32 [num_seqs, num_heads] or NULL
+ *
+ * Supported: head_dim a multiple of 4 up to 512.
+ */
+int metis_merge_attn_states(const float* part_out, const float* part_lse, const int32_t* seq_lens,
+                            int partition_size, void* out, float* lse_out,
+                            int num_seqs, int num_heads, int head_dim, int max_parts,
+                            int out_dtype, void* stream);
+
+/*
+ * metis_read_status -- the device status word (METIS_STATUS_* bits, OR-ed
+ * over every launch since it was last cleared) of the current device.
+ * Synchronises the device: for tests and debugging, not for the hot path.
+ * clear != 0 resets it to 0.  Returns METIS_OK or METIS_E_CUDA.
+ */
+int metis_read_status(uint32_t* status_out, int clear);
+
+/* Message for the last non-zero return on the calling thread ("" if none). */
+const char* metis_last_error(void);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int metis_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* METIS_ATTN_H */

@@ -30,8 +30,9 @@ and writes that definition out directly:
 6. Split-KV: the same softmax over each partition of a sequence's tokens,
    then the log-sum-exp merge of the partial results.
 
-Inputs are NumPy arrays (or anything ``np.asarray`` accepts); floating inputs
-are converted to float64 exactly (bf16 and fp32 values are representable).
+Inputs are NumPy arrays or CPU torch tensors (NumPy has no bf16); the rows
+that are used are converted to float64 exactly (bf16 and fp32 values are
+representable).
 No blocking, fusion or reordering beyond a library matrix product per
 (sequence, kv head).
 """
@@ -39,12 +40,27 @@ No blocking, fusion or reordering beyond a library matrix product per
 from __future__ import annotations
 
 import numpy as np
+import torch
 
 NEG_INF = -np.inf
 
 
 def _f64(x) -> np.ndarray:
+    """float64 copy of an array or a torch tensor (bf16 and fp32 values convert exactly)."""
+    if isinstance(x, torch.Tensor):
+        return x.detach().to("cpu", torch.float64).numpy()
     return np.asarray(x, dtype=np.float64)
+
+
+def _arr(x):
+    """Index-only access: torch tensors stay tensors (NumPy has no bf16), the rest become arrays."""
+    return x if isinstance(x, torch.Tensor) else np.asarray(x)
+
+
+def _ints(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        return x.detach().cpu().numpy()
+    return np.asarray(x)
 
 
 def gather_tokens(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int, block_size: int) -> np.ndarray:
@@ -55,10 +71,12 @@ def gather_tokens(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int, 
     table entries are read, and only slots below ``seq_len``.
     """
     t = np.arange(int(seq_len))
-    phys = np.asarray(block_table_row)[t // block_size].astype(np.int64)
+    phys = _ints(block_table_row)[t // block_size].astype(np.int64)
     slot = t % block_size
     if len(t) and (phys.min() < 0 or phys.max() >= cache.shape[0]):
         raise IndexError("block table entry outside the block pool")
+    if isinstance(cache, torch.Tensor):
+        return cache[torch.from_numpy(phys), torch.from_numpy(slot)]
     return cache[phys, slot]
 
 
@@ -107,8 +125,8 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale):
     last cached position, so it sees all ``seq_lens[s]`` tokens.
     """
     q = _f64(q)
-    k_cache = np.asarray(k_cache)
-    v_cache = np.asarray(v_cache)
+    k_cache = _arr(k_cache)
+    v_cache = _arr(v_cache)
     S, H, D = q.shape
     bs, G = k_cache.shape[1], k_cache.shape[2]
     if H % G:
@@ -116,9 +134,9 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale):
     r = H // G
     out = np.zeros((S, H, v_cache.shape[3]), dtype=np.float64)
     lse = np.full((S, H), NEG_INF, dtype=np.float64)
-    bt = np.asarray(block_table)
+    bt = _ints(block_table)
     for s in range(S):
-        L = int(seq_lens[s])
+        L = int(_ints(seq_lens)[s])
         if L <= 0:
             continue
         for g in range(G):
@@ -141,21 +159,21 @@ def paged_prefill(q, cu_q_lens, k_cache, v_cache, block_table, seq_lens, scale):
     lse [T, H])``.
     """
     q = _f64(q)
-    k_cache = np.asarray(k_cache)
-    v_cache = np.asarray(v_cache)
+    k_cache = _arr(k_cache)
+    v_cache = _arr(v_cache)
     T, H, D = q.shape
     bs, G = k_cache.shape[1], k_cache.shape[2]
     if H % G:
         raise ValueError("q heads must be a multiple of kv heads")
     r = H // G
-    cu = np.asarray(cu_q_lens, dtype=np.int64)
-    bt = np.asarray(block_table)
+    cu = _ints(cu_q_lens).astype(np.int64)
+    bt = _ints(block_table)
     out = np.zeros((T, H, v_cache.shape[3]), dtype=np.float64)
     lse = np.full((T, H), NEG_INF, dtype=np.float64)
     for s in range(len(cu) - 1):
         q0, q1 = int(cu[s]), int(cu[s + 1])
         q_len = q1 - q0
-        L = int(seq_lens[s])
+        L = int(_ints(seq_lens)[s])
         if q_len <= 0:
             continue
         if q_len > L:
@@ -177,20 +195,20 @@ def paged_prefill_rows(q, cu_q_lens, k_cache, v_cache, block_table, seq_lens, sc
     Used to check sampled outputs of full-size workloads.  Returns
     ``(out [n, D], lse [n])`` in the order of ``rows``.
     """
-    q = np.asarray(q)
-    k_cache = np.asarray(k_cache)
-    v_cache = np.asarray(v_cache)
+    q = _arr(q)
+    k_cache = _arr(k_cache)
+    v_cache = _arr(v_cache)
     H = q.shape[1]
     bs, G = k_cache.shape[1], k_cache.shape[2]
     r = H // G
-    cu = np.asarray(cu_q_lens, dtype=np.int64)
-    bt = np.asarray(block_table)
+    cu = _ints(cu_q_lens).astype(np.int64)
+    bt = _ints(block_table)
     out = np.zeros((len(rows), v_cache.shape[3]))
     lse = np.full(len(rows), NEG_INF)
     for n, (tok, h) in enumerate(rows):
         s = int(np.searchsorted(cu, tok, side="right") - 1)
         q_len = int(cu[s + 1] - cu[s])
-        L = int(seq_lens[s])
+        L = int(_ints(seq_lens)[s])
         i = int(tok - cu[s])
         g = h // r
         K = _f64(gather_tokens(k_cache[:, :, g], bt[s], L, bs))
@@ -209,14 +227,14 @@ def mla_decode(q, kv_cache, block_table, seq_lens, scale, d_latent=512):
     columns.  Returns ``(out [S, H, d_latent], lse [S, H])``.
     """
     q = _f64(q)
-    kv_cache = np.asarray(kv_cache)
+    kv_cache = _arr(kv_cache)
     S, H, dq = q.shape
     bs = kv_cache.shape[1]
-    bt = np.asarray(block_table)
+    bt = _ints(block_table)
     out = np.zeros((S, H, d_latent), dtype=np.float64)
     lse = np.full((S, H), NEG_INF, dtype=np.float64)
     for s in range(S):
-        L = int(seq_lens[s])
+        L = int(_ints(seq_lens)[s])
         if L <= 0:
             continue
         rows = _f64(gather_tokens(kv_cache, bt[s], L, bs))   # [L, dq]
@@ -263,7 +281,8 @@ def merge_states(o_parts, lse_parts):
     total = w.sum(axis=0)
     lse = np.where(finite, m_safe + np.log(np.where(finite, total, 1.0)), NEG_INF)
     coef = np.where(finite[None], w / np.where(finite, total, 1.0)[None], 0.0)
-    out = (coef[..., None] * o_parts).sum(axis=0)
+    # an empty partition's output is undefined (it was never written): skip it, don't multiply it by 0
+    out = np.where(coef[..., None] > 0, coef[..., None] * o_parts, 0.0).sum(axis=0)
     return out, lse
 
 
@@ -274,16 +293,16 @@ def paged_decode_split(q, k_cache, v_cache, block_table, seq_lens, scale, partit
     indexed ``[s][g]``.
     """
     q = _f64(q)
-    k_cache = np.asarray(k_cache)
-    v_cache = np.asarray(v_cache)
+    k_cache = _arr(k_cache)
+    v_cache = _arr(v_cache)
     S, H, D = q.shape
     bs, G = k_cache.shape[1], k_cache.shape[2]
     r = H // G
-    bt = np.asarray(block_table)
+    bt = _ints(block_table)
     out = np.zeros((S, H, v_cache.shape[3]))
     lse = np.full((S, H), NEG_INF)
     for s in range(S):
-        L = int(seq_lens[s])
+        L = int(_ints(seq_lens)[s])
         if L <= 0:
             continue
         for g in range(G):

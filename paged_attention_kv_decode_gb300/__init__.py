@@ -1,1 +1,29 @@
-"""GB300-native paged attention over a paged KV cache (binding loaded lazily)."""
+"""GB300-native attention over a paged KV cache.
+
+The compute lives in ``lib/libmetis_attn.so`` (hand-written CUDA for sm_103a,
+C ABI declared in ``include/metis_attn.h``); this package holds its ctypes
+binding, the in-tree build script and the seeded workload generator.  The
+library is loaded on first use; a missing library raises instead of falling
+back to any other implementation.
+"""
+
+from ._binding import (  # noqa: F401
+    LIB_PATH,
+    METIS_BF16,
+    METIS_F32,
+    SIGNATURES,
+    STATUS_BAD_BLOCK_ID,
+    STATUS_BAD_Q_LEN,
+    STATUS_SEQ_TOO_LONG,
+    STATUS_WAIT_TIMEOUT,
+    MetisError,
+    load_library,
+    metis_decode_workspace_bytes,
+    metis_last_error,
+    metis_merge_attn_states,
+    metis_paged_attn_decode,
+    metis_paged_attn_decode_partials,
+    split_workspace_views,
+    metis_read_status,
+    metis_version,
+)

@@ -1,0 +1,242 @@
+"""ctypes binding of ``libmetis_attn.so`` -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but check the torch tensors it is handed (device, dtype, shape,
+contiguity), allocate outputs / workspace with torch when the caller did not
+pass them, and hand raw device pointers plus the current CUDA stream to the
+library.  All computation happens in the library's CUDA kernels; there is no
+CPU or PyTorch fallback: a missing library or a CPU tensor raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libmetis_attn.so")
+
+METIS_F32 = 0
+METIS_BF16 = 1
+
+STATUS_BAD_BLOCK_ID = 1
+STATUS_SEQ_TOO_LONG = 2
+STATUS_WAIT_TIMEOUT = 4
+STATUS_BAD_Q_LEN = 8
+
+_ERRORS = {
+    -1: "METIS_E_NULL",
+    -2: "METIS_E_SHAPE",
+    -3: "METIS_E_UNSUPPORTED",
+    -4: "METIS_E_ALIGN",
+    -5: "METIS_E_WORKSPACE",
+    -6: "METIS_E_CUDA",
+}
+
+
+class MetisError(RuntimeError):
+    """A non-zero status from the library; ``code`` is the METIS_E_* value."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{_ERRORS.get(code, code)}: {message}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_f = ctypes.c_float
+
+# name -> (restype, argtypes); mirrors include/metis_attn.h
+SIGNATURES = {
+    "metis_paged_attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                                     _vp, _sz, _vp]),
+    "metis_paged_attn_decode_partials": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                                              _vp, _sz, _vp]),
+    "metis_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "metis_merge_attn_states": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "metis_read_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
+    "metis_last_error": (ctypes.c_char_p, []),
+    "metis_version": (_i, []),
+}
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the library once (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not found at {path}: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise MetisError(rc, load_library().metis_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return METIS_F32
+    if dt == torch.bfloat16:
+        return METIS_BF16
+    raise TypeError(f"unsupported dtype {dt}; use float32 or bfloat16")
+
+
+def _cuda(name: str, t: torch.Tensor, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def metis_version() -> int:
+    return load_library().metis_version()
+
+
+def metis_last_error() -> str:
+    return load_library().metis_last_error().decode()
+
+
+def metis_read_status(clear: bool = True) -> int:
+    """The device status word (METIS_STATUS_* bits); synchronises the device."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().metis_read_status(ctypes.byref(v), int(bool(clear))))
+    return int(v.value)
+
+
+def metis_decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_seq_len: int,
+                                 partition_size: int) -> int:
+    return int(load_library().metis_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_seq_len,
+                                                           partition_size))
+
+
+def metis_paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
+                            out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                            partition_size: int = 0, max_seq_len: Optional[int] = None,
+                            workspace: Optional[torch.Tensor] = None, stream=None,
+                            want_lse: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Paged decode; returns ``(out, lse_out)``.  ``max_seq_len=None`` reads seq_lens (a sync)."""
+    lib = load_library()
+    _cuda("q", q, ndim=3)
+    dt = _dtype_code(q.dtype)
+    _cuda("k_cache", k_cache, dtype=q.dtype, ndim=4)
+    _cuda("v_cache", v_cache, dtype=q.dtype, ndim=4)
+    _cuda("block_table", block_table, dtype=torch.int32, ndim=2)
+    _cuda("seq_lens", seq_lens, dtype=torch.int32, ndim=1)
+    S, H, D = q.shape
+    nb, bs, G, Dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or Dk != D or block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, dtype=q.dtype, ndim=3)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((S, H), dtype=torch.float32, device=q.device)
+    if lse_out is not None:
+        _cuda("lse_out", lse_out, dtype=torch.float32, ndim=2)
+    if max_seq_len is None:
+        max_seq_len = max(1, int(seq_lens.max().item())) if S else 1
+    need = metis_decode_workspace_bytes(S, H, D, max_seq_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.metis_paged_attn_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse_out),
+        S, H, G, D, bs, block_table.shape[1], nb, dt, float(scale), int(partition_size), int(max_seq_len),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, lse_out
+
+
+def metis_merge_attn_states(part_out: torch.Tensor, part_lse: torch.Tensor, seq_lens: torch.Tensor,
+                            partition_size: int, *, out: Optional[torch.Tensor] = None,
+                            lse_out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+                            stream=None, want_lse: bool = False):
+    """Log-sum-exp merge of ``part_out`` [S, H, P, D] / ``part_lse`` [S, H, P]; returns ``(out, lse_out)``."""
+    lib = load_library()
+    _cuda("part_out", part_out, dtype=torch.float32, ndim=4)
+    _cuda("part_lse", part_lse, dtype=torch.float32, ndim=3)
+    _cuda("seq_lens", seq_lens, dtype=torch.int32, ndim=1)
+    S, H, P, D = part_out.shape
+    if part_lse.shape != (S, H, P) or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((S, H, D), dtype=out_dtype, device=part_out.device)
+    _cuda("out", out, ndim=3)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((S, H), dtype=torch.float32, device=part_out.device)
+    _check(lib.metis_merge_attn_states(_ptr(part_out), _ptr(part_lse), _ptr(seq_lens), int(partition_size),
+                                       _ptr(out), _ptr(lse_out), S, H, D, P, _dtype_code(out.dtype),
+                                       _stream(stream)))
+    return out, lse_out
+
+
+def split_workspace_views(workspace: torch.Tensor, num_seqs: int, num_heads: int, head_dim: int, max_seq_len: int,
+                          partition_size: int):
+    """``(part_out, part_lse)`` views of a split-KV decode workspace (the layout the header documents)."""
+    parts = -(-max_seq_len // partition_size)
+    units = num_seqs * num_heads * parts
+    off = -(-units * head_dim * 4 // 256) * 256
+    flat = workspace.view(torch.uint8)
+    part_out = flat[:units * head_dim * 4].view(torch.float32).view(num_seqs, num_heads, parts, head_dim)
+    part_lse = flat[off:off + units * 4].view(torch.float32).view(num_seqs, num_heads, parts)
+    return part_out, part_lse
+
+
+def metis_paged_attn_decode_partials(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                     block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
+                                     partition_size: int, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
+                                     stream=None) -> torch.Tensor:
+    """Split-KV partials into ``workspace`` (allocated when None); returns the workspace."""
+    lib = load_library()
+    _cuda("q", q, ndim=3)
+    dt = _dtype_code(q.dtype)
+    _cuda("k_cache", k_cache, dtype=q.dtype, ndim=4)
+    _cuda("v_cache", v_cache, dtype=q.dtype, ndim=4)
+    _cuda("block_table", block_table, dtype=torch.int32, ndim=2)
+    _cuda("seq_lens", seq_lens, dtype=torch.int32, ndim=1)
+    S, H, D = q.shape
+    nb, bs, G, _ = k_cache.shape
+    need = metis_decode_workspace_bytes(S, H, D, max_seq_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.metis_paged_attn_decode_partials(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), S, H, G, D, bs,
+        block_table.shape[1], nb, dt, float(scale), int(partition_size), int(max_seq_len), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+    return workspace

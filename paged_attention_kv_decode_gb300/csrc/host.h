@@ -1,0 +1,35 @@
+// Host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace metis {
+
+// Record a message for metis_last_error() and return `code`.
+int fail(int code, const char* fmt, ...);
+void clear_error();
+
+// cudaGetLastError() after a launch: METIS_OK, or METIS_E_CUDA with a message.
+int check_launch(const char* what);
+
+// Encode a tiled TMA descriptor (cuTensorMapEncodeTiled, fetched from the
+// driver at run time).  dims / box are innermost first; strides are the byte
+// strides of dims 1..rank-1.  Returns METIS_OK or an error code.
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle);
+
+// Raise a kernel's dynamic shared memory limit once per device.
+int set_max_dynamic_smem(const void* func, int bytes, int* done_mask);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per-translation-unit device status words.
+int decode_status(uint32_t* bits, int clear);
+
+}  // namespace metis

@@ -1,0 +1,140 @@
+"""The C ABI: every declared symbol is exported, and bad arguments are rejected on the host.
+
+These tests run without a GPU.  Every call below is one the library must
+reject before touching CUDA, so nothing is ever launched with the fake
+pointers used here.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_attention_kv_decode_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = []
+    for fname in sorted(os.listdir(HEADER_DIR)):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(metis_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(pa.LIB_PATH):
+        from paged_attention_kv_decode_gb300 import build
+        build.build()
+    return pa.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("metis_paged_attn_decode", "metis_paged_attn_decode_partials", "metis_merge_attn_states", "metis_decode_workspace_bytes",
+              "metis_read_status", "metis_last_error", "metis_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_binding_covers_every_declared_symbol():
+    assert sorted(pa.SIGNATURES) == declared_functions()
+
+
+def test_version(lib):
+    assert pa.metis_version() >= 100
+
+
+def test_workspace_bytes(lib):
+    assert pa.metis_decode_workspace_bytes(4, 8, 128, 1000, 0) == 0
+    n = pa.metis_decode_workspace_bytes(4, 8, 128, 1000, 512)   # 2 partitions
+    units = 4 * 8 * 2
+    assert n >= units * 128 * 4 + units * 4 and n % 256 == 0
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced: every call below is rejected first
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, out=FAKE, lse=None, S=4, H=32, G=8, D=128, bs=16,
+             max_blocks=8, num_blocks=64, dtype=pa.METIS_BF16, scale=0.088, P=0, max_len=128, ws=None,
+             ws_bytes=0, stream=None)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.metis_paged_attn_decode(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["bt"]), vp(a["sl"]), vp(a["out"]),
+                                       vp(a["lse"]), a["S"], a["H"], a["G"], a["D"], a["bs"], a["max_blocks"],
+                                       a["num_blocks"], a["dtype"], a["scale"], a["P"], a["max_len"], vp(a["ws"]),
+                                       a["ws_bytes"], vp(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(bt=None), -1), (dict(out=None), -1),
+    (dict(S=-1), -2), (dict(H=0), -2), (dict(max_len=0), -2), (dict(num_blocks=0), -2),
+    (dict(H=30), -2),                                   # not a multiple of kv heads
+    (dict(D=96), -3), (dict(bs=8), -3), (dict(dtype=7), -3),
+    (dict(H=48, G=4), -3),                              # ratio 12 > 8
+    (dict(H=24, G=8), -3),                              # bf16 ratio 3
+    (dict(q=FAKE + 2), -4), (dict(k=FAKE + 8), -4), (dict(sl=FAKE + 1), -4),
+    (dict(P=100), -2), (dict(P=-16), -2),
+    (dict(P=512, max_len=100_000), -5),                 # split needs a workspace
+    (dict(P=512, ws=FAKE, ws_bytes=16), -5),            # too small
+    (dict(scale=float("nan")), -2),
+    (dict(max_blocks=1 << 28, bs=64), -2),              # max_blocks * bs overflows int32
+    (dict(S=70000), -2),
+])
+def test_decode_rejects(lib, kw, code):
+    assert _decode(lib, **kw) == code
+    assert pa.metis_last_error() != ""
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    assert _decode(lib, S=0) == 0
+    assert pa.metis_last_error() == ""
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(po=None), -1), (dict(D=130), -3), (dict(D=1024), -3), (dict(P=0), -2), (dict(dt=3), -3),
+    (dict(po=FAKE + 4), -4),
+])
+def test_merge_rejects(lib, kw, code):
+    a = dict(po=FAKE, pl=FAKE, sl=FAKE, P=512, out=FAKE, lse=None, S=2, H=4, D=128, maxp=3, dt=pa.METIS_BF16)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    rc = lib.metis_merge_attn_states(vp(a["po"]), vp(a["pl"]), vp(a["sl"]), a["P"], vp(a["out"]), vp(a["lse"]),
+                                     a["S"], a["H"], a["D"], a["maxp"], a["dt"], None)
+    assert rc == code
+
+
+def test_read_status_rejects_null(lib):
+    assert lib.metis_read_status(None, 0) == -1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 4, 64)
+    kc = torch.zeros(2, 16, 1, 64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pa.metis_paged_attn_decode(q, kc, kc, torch.zeros(1, 1, dtype=torch.int32),
+                                   torch.ones(1, dtype=torch.int32), 0.1, max_seq_len=1)
+
+
+def test_partials_reject(lib):
+    vp = ctypes.c_void_p
+    f = lib.metis_paged_attn_decode_partials
+    # partition_size 0 is meaningless for partials
+    assert f(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 4, 32, 8, 128, 16, 8, 64, pa.METIS_BF16, 0.1, 0, 128,
+             vp(FAKE), 1 << 20, None) == -2
+    # workspace too small
+    assert f(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 4, 32, 8, 128, 16, 8, 64, pa.METIS_BF16, 0.1, 64, 128,
+             vp(FAKE), 64, None) == -5

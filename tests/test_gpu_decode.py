@@ -1,0 +1,228 @@
+"""GPU parity of paged decode and the split-KV merge against the float64 oracle.
+
+All calls go through the C ABI (ctypes binding).  Inputs are the seeded
+workload recipes; the pool entries the method must not read are NaN
+("poisoned") wherever a case says so, so a read through a wrong index or past
+a sequence's end shows up as a non-finite output.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_attention_kv_decode_gb300 as pa
+from paged_attention_kv_decode_gb300 import workloads as wl
+from helpers import assert_lse, assert_parity, dev, f64, replace_blocks
+
+pytestmark = pytest.mark.gpu
+
+# the partition size bench.py uses for the batched-decode workload
+BENCH_PARTITION = 512
+
+
+@pytest.fixture(autouse=True)
+def _clear_status():
+    if torch.cuda.is_available():
+        pa.metis_read_status(clear=True)
+    yield
+
+
+def oracle_decode(case):
+    return oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale)
+
+
+def gpu_decode(case, partition_size=0, max_seq_len=None, block_table=None, k_cache=None, v_cache=None):
+    out, lse = pa.metis_paged_attn_decode(
+        dev(case.q), dev(case.k_cache if k_cache is None else k_cache),
+        dev(case.v_cache if v_cache is None else v_cache),
+        dev(case.block_table if block_table is None else block_table), dev(case.seq_lens), case.scale,
+        partition_size=partition_size, max_seq_len=max_seq_len or max(1, case.max_seq_len), want_lse=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check_case(case, partition_size=0):
+    ref_o, ref_l = oracle_decode(case)
+    out, lse = gpu_decode(case, partition_size)
+    err = assert_parity(out, ref_o, case.dtype)
+    assert_lse(lse, ref_l, case.dtype)
+    assert pa.metis_read_status() == 0
+    return err
+
+
+# ---------------------------------------------------------------------------
+# tiny fp32 workload (1e-5)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("poison", [False, True])
+@pytest.mark.parametrize("partition_size", [0, 16, 32])
+def test_tiny_fp32_decode(poison, partition_size):
+    check_case(wl.config1_tiny_decode(poison=poison), partition_size)
+
+
+@pytest.mark.parametrize("D,bs,H,G", [(64, 16, 8, 8), (128, 32, 8, 1), (128, 64, 12, 2), (64, 32, 6, 3)])
+def test_fp32_shapes(D, bs, H, G):
+    lens = [1, 15, 16, 17, 63, 64, 65, 200]
+    case = wl.make_decode_case(40 + D + bs, lens, H=H, G=G, D=D, bs=bs, dtype=torch.float32, extra_blocks=4,
+                               poison=True)
+    check_case(case, 0)
+    check_case(case, 64)
+
+
+# ---------------------------------------------------------------------------
+# bf16 decode: boundaries, split sizes, shapes
+# ---------------------------------------------------------------------------
+
+EDGE_LENS = [1, 15, 16, 17, 511, 512, 513, 100, 1000, 2047]
+
+
+@pytest.mark.parametrize("partition_size", [0, 64, 128, 512, 4096])
+def test_bf16_edge_lengths(partition_size):
+    case = wl.make_decode_case(77, EDGE_LENS, H=32, G=8, D=128, bs=16, dtype=torch.bfloat16, extra_blocks=7,
+                               poison=True)
+    check_case(case, partition_size)
+
+
+@pytest.mark.parametrize("D,bs,H,G", [(64, 16, 8, 8), (128, 32, 16, 8), (128, 64, 16, 2), (64, 64, 32, 4),
+                                      (128, 16, 8, 1)])
+def test_bf16_shapes(D, bs, H, G):
+    case = wl.make_decode_case(90 + D + bs + H, [1, 16, 33, 64, 65, 300, 777], H=H, G=G, D=D, bs=bs,
+                               dtype=torch.bfloat16, extra_blocks=3, poison=True)
+    check_case(case, 0)
+    check_case(case, 128)
+
+
+def test_batched_decode_recipe_small():
+    """The batched-decode recipe with fewer, shorter sequences (several tiles, ragged tails)."""
+    case = wl.config2_batched_decode(poison=True, num_seqs=12, len_lo=17, len_hi=1500, extra_blocks=9)
+    check_case(case, 0)
+    check_case(case, BENCH_PARTITION)
+
+
+def test_split_sizes_agree():
+    case = wl.make_decode_case(5, [3000, 1234, 16, 4097], H=32, G=8, D=128, bs=16, dtype=torch.bfloat16)
+    outs = [gpu_decode(case, P)[0].float() for P in (128, 512, 4096)]
+    ref, _ = oracle_decode(case)
+    for o in outs:
+        assert_parity(o, ref, torch.bfloat16)
+
+
+def test_block_permutation_is_bitwise_invariant():
+    case = wl.config2_batched_decode(num_seqs=6, len_lo=100, len_hi=900, extra_blocks=20)
+    base, base_lse = gpu_decode(case, BENCH_PARTITION)
+    for seed in (1, 2):
+        k2, v2, bt2 = replace_blocks(case.k_cache, case.v_cache, case.block_table, case.seq_lens, seed)
+        out, lse = gpu_decode(case, BENCH_PARTITION, block_table=bt2, k_cache=k2, v_cache=v2)
+        assert torch.equal(out, base) and torch.equal(lse, base_lse)
+
+
+def test_repeat_runs_are_bitwise_equal():
+    case = wl.config2_batched_decode(num_seqs=8, len_lo=500, len_hi=3000)
+    a = gpu_decode(case, BENCH_PARTITION)
+    b = gpu_decode(case, BENCH_PARTITION)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_empty_sequence_gives_zero_and_neg_inf():
+    case = wl.make_decode_case(8, [0, 5, 0, 40], H=8, G=2, D=128, bs=16, dtype=torch.bfloat16, extra_blocks=2)
+    for P in (0, 16):
+        out, lse = gpu_decode(case, P, max_seq_len=40)
+        o = out.float().cpu()
+        assert (o[0] == 0).all() and (o[2] == 0).all()
+        assert torch.isinf(lse[0]).all() and (lse[0] < 0).all() and torch.isinf(lse[2]).all()
+        ref_o, ref_l = oracle_decode(case)
+        assert_parity(out, ref_o, torch.bfloat16)
+        assert_lse(lse, ref_l, torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads
+# ---------------------------------------------------------------------------
+
+def test_batched_decode_full_size():
+    """64 seqs, lengths U[512, 4096], 32/8 heads, head_dim 128, block 16: every output vs the oracle."""
+    case = wl.config2_batched_decode(poison=False)
+    check_case(case, BENCH_PARTITION)
+    check_case(case, 0)
+
+
+def test_long_split_decode_full_size_sampled():
+    """8 seqs of U[32768, 131072] tokens, 512-token partitions; the oracle checks two whole sequences."""
+    case = wl.config3_long_split_decode()
+    out, lse = gpu_decode(case, case.partition_size)
+    assert pa.metis_read_status() == 0
+    o = f64(out)
+    assert np.isfinite(o).all()
+    lens = case.seq_lens.numpy()
+    for s in (int(np.argmax(lens)), int(np.argmin(lens))):
+        sub = wl.DecodeCase(name="sub", q=case.q[s:s + 1], k_cache=case.k_cache, v_cache=case.v_cache,
+                            block_table=case.block_table[s:s + 1], seq_lens=case.seq_lens[s:s + 1],
+                            scale=case.scale)
+        ref_o, ref_l = oracle_decode(sub)
+        assert_parity(out[s:s + 1], ref_o, torch.bfloat16)
+        assert_lse(lse[s:s + 1], ref_l, torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# content errors: reported in the status word, never a fault
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_is_flagged_and_read_as_zeros():
+    case = wl.make_decode_case(12, [40, 40], H=8, G=2, D=128, bs=16, dtype=torch.bfloat16)
+    bt = case.block_table.clone()
+    bt[1, 1] = case.num_blocks + 1000          # tokens 16..31 of sequence 1 point outside the pool
+    out, _ = gpu_decode(case, 0, block_table=bt)
+    assert pa.metis_read_status() & pa.STATUS_BAD_BLOCK_ID
+    ref_o, _ = oracle_decode(case)
+    assert_parity(out[:1], ref_o[:1], torch.bfloat16)   # the other sequence is untouched
+    assert torch.isfinite(out.float()).all()
+
+
+def test_bad_block_id_fp32_path():
+    case = wl.make_decode_case(13, [20], H=4, G=1, D=64, bs=16, dtype=torch.float32)
+    bt = case.block_table.clone()
+    bt[0, 0] = -7
+    out, _ = gpu_decode(case, 0, block_table=bt)
+    assert pa.metis_read_status() & pa.STATUS_BAD_BLOCK_ID
+    assert torch.isfinite(out).all()
+
+
+def test_seq_longer_than_max_seq_len_is_flagged():
+    case = wl.make_decode_case(14, [100, 30], H=8, G=2, D=128, bs=16, dtype=torch.bfloat16)
+    out, _ = gpu_decode(case, 32, max_seq_len=64)
+    assert pa.metis_read_status() & pa.STATUS_SEQ_TOO_LONG
+    assert torch.isfinite(out.float()).all()
+    ref_o, _ = oracle_decode(case)
+    assert_parity(out[1:], ref_o[1:], torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# the merge entry point on its own
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128, 512])
+def test_merge_attn_states_against_oracle(D):
+    rng = np.random.default_rng(D)
+    S, H, P, psize = 5, 6, 7, 64
+    part_out = rng.standard_normal((S, H, P, D)).astype(np.float32)
+    part_lse = (rng.standard_normal((S, H, P)) * 3).astype(np.float32)
+    lens = np.array([1, 64, 65, 448, 0], dtype=np.int32)     # 1, 1, 2, 7, 0 partitions
+    part_lse[3, :, 4] = -np.inf                               # an empty partition inside the range
+    part_out[3, :, 4] = np.nan                                # ... whose output must not be read
+    part_out[0, :, 1:] = np.nan                               # partitions past the length
+    out, lse = pa.metis_merge_attn_states(torch.from_numpy(part_out).cuda(), torch.from_numpy(part_lse).cuda(),
+                                          torch.from_numpy(lens).cuda(), psize, want_lse=True)
+    torch.cuda.synchronize()
+    for s in range(S):
+        n = min(P, -(-int(lens[s]) // psize)) if lens[s] > 0 else 0
+        if n == 0:
+            ref_o = np.zeros((H, D))
+            ref_l = np.full(H, -np.inf)
+        else:
+            ref_o, ref_l = oracle.merge_states(part_out[s, :, :n].transpose(1, 0, 2).astype(np.float64),
+                                               part_lse[s, :, :n].T.astype(np.float64))
+        assert_parity(out[s], ref_o, torch.float32)
+        assert_lse(lse[s], ref_l, torch.float32)

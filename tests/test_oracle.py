@@ -342,8 +342,10 @@ def test_merge_closed_forms():
     out, lse = oracle.merge_states(o, np.array([[0.5], [0.5]]))
     np.testing.assert_allclose(out[0], [2.0, 4.0], rtol=0, atol=1e-15)
     assert abs(lse[0] - (0.5 + math.log(2.0))) < 1e-15
-    # an empty partition weighs nothing
-    out, lse = oracle.merge_states(o, np.array([[-np.inf], [1.25]]))
+    # an empty partition weighs nothing, whatever its (never written) output holds
+    o_nan = o.copy()
+    o_nan[0] = np.nan
+    out, lse = oracle.merge_states(o_nan, np.array([[-np.inf], [1.25]]))
     np.testing.assert_allclose(out[0], [3.0, 6.0], rtol=0, atol=0)
     assert lse[0] == 1.25
     # all empty: zero output, -inf lse
