@@ -288,12 +288,18 @@ def run_ours(args, world, rank, local):
     ev_mid = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(str(getattr(props, "uuid", "")))
     sampler.start()
-    # clock ramp (untimed), then W warm-up steps
-    t_end = time.time() + 1.0
-    while time.time() < t_end:
-        for _ in range(20):
+    # clock ramp (untimed; ~1 s, or a fixed number of steps so that profiler launch indices are fixed),
+    # then W warm-up steps
+    if args.ramp_steps is not None:
+        for _ in range(args.ramp_steps):
             step()
         torch.cuda.synchronize()
+    else:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -398,6 +404,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=PARTITION)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ramp-steps", type=int, default=None,
+                    help="untimed steps before warm-up (default: about one second of steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3 (the minimum)")
