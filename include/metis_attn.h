@@ -127,6 +127,44 @@ int metis_paged_attn_decode_partials(const void* q, const void* k_cache, const v
                                      float scale, int partition_size, int max_seq_len,
                                      void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * metis_paged_attn_decode_noalloc -- metis_paged_attn_decode for callers that
+ * cannot allocate device memory.
+ *
+ * The pages have no counterpart of this call: it exists for callers that
+ * cannot call cudaMalloc -- a host framework that owns all device memory and
+ * hands its plugins no allocator, or a latency-critical path that cannot take
+ * the implicit device synchronisation of an allocation.  Arguments and
+ * results are those of metis_paged_attn_decode, without the workspace: the
+ * split-KV partials go to a scratch array of METIS_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that the library itself declares in device memory.
+ *
+ *  - Nothing is allocated or freed: no cudaMalloc / cudaFree, no allocating
+ *    library routine.  The caller still passes q, the caches, the tables and
+ *    out / lse_out.
+ *  - Every GPU that loads the library holds the 64 MiB until the process
+ *    exits.
+ *  - A split that needs more than METIS_NOALLOC_SCRATCH_BYTES
+ *    (metis_decode_workspace_bytes(...) > the limit) is rejected with
+ *    METIS_E_WORKSPACE and nothing is launched.  partition_size 0 needs no
+ *    scratch.
+ *  - The first call on a device looks up the array's device address for that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - Every call shares the one array.  Calls whose work overlaps on the GPU
+ *    (other streams, other threads, without ordering between them) race on
+ *    it and give wrong results; calls in one stream are ordered and safe.
+ *    The array keeps the last call's contents; nothing in it needs clearing,
+ *    because each call writes every partial it reads.
+ */
+#define METIS_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int metis_paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table, const int32_t* seq_lens,
+                                    void* out, float* lse_out,
+                                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int max_blocks, int num_blocks, int dtype,
+                                    float scale, int partition_size, int max_seq_len, void* stream);
+
 /* Bytes of workspace metis_paged_attn_decode needs (0 when partition_size == 0). */
 size_t metis_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                     int max_seq_len, int partition_size);

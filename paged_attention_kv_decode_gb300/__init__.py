@@ -21,7 +21,9 @@ from ._binding import (  # noqa: F401
     metis_decode_workspace_bytes,
     metis_last_error,
     metis_merge_attn_states,
+    NOALLOC_SCRATCH_BYTES,
     metis_paged_attn_decode,
+    metis_paged_attn_decode_noalloc,
     metis_paged_attn_decode_partials,
     split_workspace_views,
     metis_read_status,

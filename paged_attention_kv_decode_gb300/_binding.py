@@ -60,6 +60,8 @@ SIGNATURES = {
                                      _vp, _sz, _vp]),
     "metis_paged_attn_decode_partials": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
                                               _vp, _sz, _vp]),
+    "metis_paged_attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
+                                             _i, _i, _vp]),
     "metis_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "metis_merge_attn_states": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "metis_read_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
@@ -240,3 +242,36 @@ def metis_paged_attn_decode_partials(q: torch.Tensor, k_cache: torch.Tensor, v_c
         block_table.shape[1], nb, dt, float(scale), int(partition_size), int(max_seq_len), _ptr(workspace), ws_bytes,
         _stream(stream)))
     return workspace
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def metis_paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                    block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
+                                    out: torch.Tensor, lse_out: Optional[torch.Tensor] = None,
+                                    partition_size: int = 0, max_seq_len: int, stream=None):
+    """Paged decode whose split-KV scratch is the library's static device array.
+
+    For callers that cannot allocate device memory: this wrapper allocates
+    nothing either, so ``out`` (and ``lse_out`` if wanted) must be passed in
+    and ``max_seq_len`` must be given.  Calls that overlap on the GPU share
+    the one scratch array and race; calls on one stream are ordered.
+    """
+    lib = load_library()
+    _cuda("q", q, ndim=3)
+    dt = _dtype_code(q.dtype)
+    _cuda("k_cache", k_cache, dtype=q.dtype, ndim=4)
+    _cuda("v_cache", v_cache, dtype=q.dtype, ndim=4)
+    _cuda("block_table", block_table, dtype=torch.int32, ndim=2)
+    _cuda("seq_lens", seq_lens, dtype=torch.int32, ndim=1)
+    _cuda("out", out, dtype=q.dtype, ndim=3)
+    if lse_out is not None:
+        _cuda("lse_out", lse_out, dtype=torch.float32, ndim=2)
+    S, H, D = q.shape
+    nb, bs, G, _ = k_cache.shape
+    _check(lib.metis_paged_attn_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse_out),
+        S, H, G, D, bs, block_table.shape[1], nb, dt, float(scale), int(partition_size), int(max_seq_len),
+        _stream(stream)))
+    return out, lse_out

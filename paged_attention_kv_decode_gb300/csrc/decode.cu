@@ -25,6 +25,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "../../include/metis_attn.h"
 #include "common.cuh"
@@ -733,4 +734,68 @@ extern "C" int metis_merge_attn_states(const float* part_out, const float* part_
     return fail(METIS_E_ALIGN, "misaligned pointer");
   return launch_merge(part_out, part_lse, seq_lens, partition_size, out, lse_out, num_seqs, num_heads, head_dim,
                       max_parts, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Decode with the library's own static scratch, for callers that cannot
+// allocate device memory.
+// ---------------------------------------------------------------------------
+namespace metis {
+
+// Split-KV partials (part_out + part_lse) of one call.  Module-scope device
+// memory: every GPU that loads the library holds these bytes until the process
+// exits.  All calls share it, and it keeps whatever the last call left; the
+// decode writes every partial the merge reads, so nothing needs clearing.
+constexpr size_t kNoAllocScratchBytes = METIS_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// The array's name is only a host-side stand-in in host code: its device
+// address is looked up once per device (with that device current) and cached.
+constexpr int kNoAllocMaxDevices = 64;
+static void* g_noalloc_ptr[kNoAllocMaxDevices];
+static std::mutex g_noalloc_mu;
+
+static int noalloc_scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(METIS_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(METIS_E_UNSUPPORTED, "device ordinal %d: the static scratch serves devices 0..%d", dev,
+                kNoAllocMaxDevices - 1);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return fail(METIS_E_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return METIS_OK;
+}
+
+}  // namespace metis
+
+extern "C" int metis_paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                               const int32_t* block_table, const int32_t* seq_lens, void* out,
+                                               float* lse_out, int num_seqs, int num_heads, int num_kv_heads,
+                                               int head_dim, int block_size, int max_blocks, int num_blocks,
+                                               int dtype, float scale, int partition_size, int max_seq_len,
+                                               void* stream) {
+  clear_error();
+  const size_t need = metis_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_seq_len, partition_size);
+  if (need > kNoAllocScratchBytes)
+    return fail(METIS_E_WORKSPACE,
+                "split-KV scratch of %zu bytes needed; the static scratch holds %zu bytes (use a larger "
+                "partition_size, a smaller batch, or metis_paged_attn_decode with your own workspace)",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (need > 0) {
+    const int rc = noalloc_scratch_address(&ws);
+    if (rc) return rc;
+    ws_bytes = kNoAllocScratchBytes;
+  }
+  return metis::paged_decode(q, k_cache, v_cache, block_table, seq_lens, out, lse_out, num_seqs, num_heads,
+                             num_kv_heads, head_dim, block_size, max_blocks, num_blocks, dtype, scale, partition_size,
+                             max_seq_len, ws, ws_bytes, stream, true);
 }
