@@ -44,7 +44,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode KV GB/s (% of HBM peak) and tokens/s; prefill TFLOP/s, 1 GB300"
 WORKLOAD = ("batched paged decode, bf16 KV: 64 seqs, seq_lens U[512,4096], 32 q / 8 kv heads, head_dim 128, "
             "block_size 16, block_table a random permutation of the pool")
-PARTITION = 512
+PARTITION = 1024
 FALLBACK_HBM_GBS = 6800.0
 
 

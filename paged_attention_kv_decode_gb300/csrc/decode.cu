@@ -261,9 +261,11 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
     const uint32_t kbase = smem_u32(smem + (warp * STAGES + st) * STAGE_BYTES);
     const uint32_t vbase = kbase + HALVES * kBoxBytes;
 
-    // S^T (16 tokens x 8 heads) = K (16 x D) . q^T (D x 8)
+    // S^T (16 tokens x 8 heads) = K (16 x D) . q^T (D x 8), in two independent
+    // accumulation chains (even / odd k-steps) to halve the dependent-MMA latency
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
     {
+      float sacc2[4] = {0.f, 0.f, 0.f, 0.f};
       const int j = lane >> 3;
       const int row = ((j & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -272,8 +274,10 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
         const uint32_t addr = kbase + (c >> 3) * kBoxBytes + row * 128 + ((((c & 7) ^ (row & 7))) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4(addr, a0, a1, a2, a3);
-        mma_bf16_16816(sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        mma_bf16_16816((kk & 1) ? sacc2 : sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i] += sacc2[i];
     }
 
     // online softmax over this unit; the thread holds tokens rA, rA+8 of heads 2*q4, 2*q4+1
@@ -567,8 +571,14 @@ static size_t split_parts(int max_seq_len, int partition_size) {
 }
 
 // bf16 decode configuration: warps per CTA and ring depth per warp.
-constexpr int kBf16Warps = 4;
-constexpr int kBf16Stages = 4;
+#ifndef METIS_DECODE_WARPS
+#define METIS_DECODE_WARPS 4
+#endif
+#ifndef METIS_DECODE_STAGES
+#define METIS_DECODE_STAGES 3
+#endif
+constexpr int kBf16Warps = METIS_DECODE_WARPS;
+constexpr int kBf16Stages = METIS_DECODE_STAGES;
 
 template <int D>
 static int launch_bf16(const DecodeParams& p, const void* k_cache, const void* v_cache, dim3 grid, cudaStream_t st) {

@@ -20,7 +20,7 @@ from helpers import assert_lse, assert_parity, dev, f64, replace_blocks
 pytestmark = pytest.mark.gpu
 
 # the partition size bench.py uses for the batched-decode workload
-BENCH_PARTITION = 512
+BENCH_PARTITION = 1024
 
 
 @pytest.fixture(autouse=True)
