@@ -170,6 +170,49 @@ size_t metis_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                     int max_seq_len, int partition_size);
 
 /*
+ * metis_paged_attn_prefill_chunk -- chunked prefill over a paged KV cache with
+ * a cached prefix (vllm-metis 0.1.0 page, introduction and "How the model maps
+ * onto vLLM -> Caches": prefix caching and chunked prefill; chunk sizes of the
+ * vllm-mblt 0.8.0 page, "Chunked Prefill Auto-Tuning"), mixed freely with
+ * single-token decodes (q_len = 1).
+ *
+ * Sequence s holds L = seq_lens[s] cached tokens whose K/V are already in the
+ * pages; its last q_len = cu_q_lens[s+1] - cu_q_lens[s] tokens are queried.
+ * Query row i of the sequence sits at position L - q_len + i and attends to
+ * every key t <= L - q_len + i: the whole cached prefix plus a causal mask
+ * inside the chunk (bottom-right aligned; with no prefix this is plain causal
+ * attention, and splitting a prompt into chunks does not change the result).
+ *
+ *   q          [num_tokens, num_heads, head_dim] bf16; the sequences' query
+ *              rows back to back, sequence s at rows cu_q_lens[s] ..
+ *   cu_q_lens  int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
+ *              cu_q_lens[num_seqs] = num_tokens
+ *   k_cache, v_cache, block_table, seq_lens   as for metis_paged_attn_decode
+ *   out        [num_tokens, num_heads, head_dim] bf16 (written)
+ *   lse_out    fp32 [num_tokens, num_heads] or NULL
+ *   max_seq_len  host-side upper bound on seq_lens
+ *   workspace  >= metis_prefill_workspace_bytes(...) bytes, 256-byte aligned,
+ *              no initialisation needed (holds the tile schedule)
+ *
+ * Supported: dtype METIS_BF16 (tensor cores: bf16 operands, fp32 accumulation);
+ * head_dim 64 or 128; block_size 16, 32 or 64; num_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}.  A q_len larger than the sequence length is clamped to it
+ * (status bit METIS_STATUS_BAD_Q_LEN).  num_seqs == 0 or num_tokens == 0 is a
+ * successful no-op.
+ */
+int metis_paged_attn_prefill_chunk(const void* q, const int32_t* cu_q_lens,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   void* out, float* lse_out,
+                                   int num_seqs, int num_tokens, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int max_blocks, int num_blocks,
+                                   int dtype, float scale, int max_seq_len,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace metis_paged_attn_prefill_chunk needs (0 for invalid sizes). */
+size_t metis_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads, int num_kv_heads);
+
+/*
  * metis_merge_attn_states -- the log-sum-exp merge of split-KV partials:
  *
  *   lse = m + ln sum_p exp(lse_p - m),  m = max_p lse_p

@@ -25,6 +25,8 @@ from ._binding import (  # noqa: F401
     metis_paged_attn_decode,
     metis_paged_attn_decode_noalloc,
     metis_paged_attn_decode_partials,
+    metis_paged_attn_prefill_chunk,
+    metis_prefill_workspace_bytes,
     split_workspace_views,
     metis_read_status,
     metis_version,

@@ -63,6 +63,9 @@ SIGNATURES = {
     "metis_paged_attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                                              _i, _i, _vp]),
     "metis_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "metis_paged_attn_prefill_chunk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                                            _i, _f, _i, _vp, _sz, _vp]),
+    "metis_prefill_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "metis_merge_attn_states": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "metis_read_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
     "metis_last_error": (ctypes.c_char_p, []),
@@ -274,4 +277,47 @@ def metis_paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_ca
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse_out),
         S, H, G, D, bs, block_table.shape[1], nb, dt, float(scale), int(partition_size), int(max_seq_len),
         _stream(stream)))
+    return out, lse_out
+
+
+def metis_prefill_workspace_bytes(num_seqs: int, num_tokens: int, num_heads: int, num_kv_heads: int) -> int:
+    return int(load_library().metis_prefill_workspace_bytes(num_seqs, num_tokens, num_heads, num_kv_heads))
+
+
+def metis_paged_attn_prefill_chunk(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                                   scale: float, *, out: Optional[torch.Tensor] = None,
+                                   lse_out: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
+                                   workspace: Optional[torch.Tensor] = None, stream=None, want_lse: bool = False):
+    """Chunked prefill (+ single-token decodes); returns ``(out, lse_out)``."""
+    lib = load_library()
+    _cuda("q", q, ndim=3)
+    dt = _dtype_code(q.dtype)
+    _cuda("cu_q_lens", cu_q_lens, dtype=torch.int32, ndim=1)
+    _cuda("k_cache", k_cache, dtype=q.dtype, ndim=4)
+    _cuda("v_cache", v_cache, dtype=q.dtype, ndim=4)
+    _cuda("block_table", block_table, dtype=torch.int32, ndim=2)
+    _cuda("seq_lens", seq_lens, dtype=torch.int32, ndim=1)
+    T, H, D = q.shape
+    nb, bs, G, Dk = k_cache.shape
+    S = seq_lens.shape[0]
+    if cu_q_lens.shape[0] != S + 1 or block_table.shape[0] != S or Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, dtype=q.dtype, ndim=3)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse_out is not None:
+        _cuda("lse_out", lse_out, dtype=torch.float32, ndim=2)
+    if max_seq_len is None:
+        max_seq_len = max(1, int(seq_lens.max().item())) if S else 1
+    need = metis_prefill_workspace_bytes(S, T, H, G)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.metis_paged_attn_prefill_chunk(
+        _ptr(q), _ptr(cu_q_lens), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out),
+        _ptr(lse_out), S, T, H, G, D, bs, block_table.shape[1], nb, dt, float(scale), int(max_seq_len),
+        _ptr(workspace), ws_bytes, _stream(stream)))
     return out, lse_out

@@ -31,5 +31,6 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 // Per-translation-unit device status words.
 int decode_status(uint32_t* bits, int clear);
+int prefill_status(uint32_t* bits, int clear);
 
 }  // namespace metis

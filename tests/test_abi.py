@@ -138,3 +138,29 @@ def test_partials_reject(lib):
     # workspace too small
     assert f(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 4, 32, 8, 128, 16, 8, 64, pa.METIS_BF16, 0.1, 64, 128,
              vp(FAKE), 64, None) == -5
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(cu=None), -1),
+    (dict(dtype=0), -3), (dict(D=96), -3), (dict(bs=8), -3), (dict(H=24, G=8), -3), (dict(H=30), -2),
+    (dict(q=FAKE + 8), -4), (dict(cu=FAKE + 2), -4),
+    (dict(ws=None), -5), (dict(ws_bytes=16), -5), (dict(ws=FAKE + 16), -5),
+    (dict(T=-1), -2), (dict(max_len=0), -2),
+])
+def test_prefill_rejects(lib, kw, code):
+    a = dict(q=FAKE, cu=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, out=FAKE, lse=None, S=4, T=100, H=32, G=8, D=128,
+             bs=16, max_blocks=8, num_blocks=64, dtype=pa.METIS_BF16, scale=0.088, max_len=128, ws=FAKE,
+             ws_bytes=1 << 20)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    rc = lib.metis_paged_attn_prefill_chunk(vp(a["q"]), vp(a["cu"]), vp(a["k"]), vp(a["v"]), vp(a["bt"]),
+                                            vp(a["sl"]), vp(a["out"]), vp(a["lse"]), a["S"], a["T"], a["H"], a["G"],
+                                            a["D"], a["bs"], a["max_blocks"], a["num_blocks"], a["dtype"], a["scale"],
+                                            a["max_len"], vp(a["ws"]), a["ws_bytes"], None)
+    assert rc == code
+
+
+def test_prefill_workspace_bytes(lib):
+    # 4 heads per group -> 32-token query tiles: ceil(100 / 32) + 4 sequences = 8 tiles of 16 bytes + header
+    assert pa.metis_prefill_workspace_bytes(4, 100, 32, 8) == 256 + 8 * 16
+    assert pa.metis_prefill_workspace_bytes(0, 100, 32, 8) == 0

@@ -1,0 +1,151 @@
+"""GPU parity of chunked prefill (prefix cache + causal chunk, mixed with decodes) against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_attention_kv_decode_gb300 as pa
+from paged_attention_kv_decode_gb300 import workloads as wl
+from helpers import assert_lse, assert_parity, dev, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clear_status():
+    if torch.cuda.is_available():
+        pa.metis_read_status(clear=True)
+    yield
+
+
+def oracle_prefill(case):
+    return oracle.paged_prefill(case.q, case.cu_q_lens, case.k_cache, case.v_cache, case.block_table,
+                                case.seq_lens, case.scale)
+
+
+def gpu_prefill(case, k_cache=None, v_cache=None, block_table=None, max_seq_len=None):
+    out, lse = pa.metis_paged_attn_prefill_chunk(
+        dev(case.q), dev(case.cu_q_lens), dev(case.k_cache if k_cache is None else k_cache),
+        dev(case.v_cache if v_cache is None else v_cache), dev(case.block_table if block_table is None else block_table),
+        dev(case.seq_lens), case.scale, max_seq_len=max_seq_len or max(1, case.max_seq_len), want_lse=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check(case):
+    ref_o, ref_l = oracle_prefill(case)
+    out, lse = gpu_prefill(case)
+    assert_parity(out, ref_o, torch.bfloat16)
+    assert_lse(lse, ref_l, torch.bfloat16)
+    assert pa.metis_read_status() == 0
+
+
+@pytest.mark.parametrize("prefix,q_len", [(0, 1), (0, 5), (0, 32), (0, 33), (0, 128), (0, 129), (1, 31),
+                                          (15, 64), (16, 100), (17, 512), (127, 1), (128, 200), (300, 77),
+                                          (1000, 256)])
+def test_single_sequence(prefix, q_len):
+    case = wl.make_prefill_case(100 + prefix + q_len, [prefix], [q_len], H=32, G=8, D=128, bs=16,
+                                dtype=torch.bfloat16, extra_blocks=3, poison=True)
+    check(case)
+
+
+@pytest.mark.parametrize("D,bs,H,G", [(128, 32, 32, 8), (128, 64, 16, 16), (64, 16, 16, 8), (64, 64, 8, 1),
+                                      (128, 16, 16, 1), (128, 16, 32, 4)])
+def test_shapes(D, bs, H, G):
+    case = wl.make_prefill_case(7 + D + bs + H, [0, 40, 129, 5, 600], [70, 1, 33, 200, 1], H=H, G=G, D=D, bs=bs,
+                                dtype=torch.bfloat16, extra_blocks=5, poison=True)
+    check(case)
+
+
+def test_chunked_prefill_recipe_small():
+    """The mixed chunk + decode recipe with fewer, shorter sequences."""
+    case = wl.config4_chunked_prefill(poison=True, num_chunks=5, chunk=160, prefix_hi=700, num_decodes=7,
+                                      dec_lo=1, dec_hi=900, extra_blocks=11)
+    check(case)
+
+
+def test_q_len_one_equals_decode():
+    case = wl.make_prefill_case(55, [0, 17, 511, 1500], [1, 1, 1, 1], H=32, G=8, D=128, bs=16,
+                                dtype=torch.bfloat16, poison=True, extra_blocks=2)
+    out, lse = gpu_prefill(case)
+    dcase = wl.DecodeCase(name="d", q=case.q, k_cache=case.k_cache, v_cache=case.v_cache,
+                          block_table=case.block_table, seq_lens=case.seq_lens, scale=case.scale)
+    d_out, d_lse = pa.metis_paged_attn_decode(dev(dcase.q), dev(dcase.k_cache), dev(dcase.v_cache),
+                                              dev(dcase.block_table), dev(dcase.seq_lens), dcase.scale,
+                                              max_seq_len=dcase.max_seq_len, want_lse=True)
+    torch.cuda.synchronize()
+    assert_parity(out, f64(d_out), torch.bfloat16)
+    assert (lse - d_lse).abs().max().item() <= 1e-3
+
+
+def test_chunking_does_not_change_rows():
+    """One 384-token chunk vs the same prompt fed as chunks of 64, 128 and 192 (the vllm-metis parity setup)."""
+    prefix, n = 200, 384
+    case = wl.make_prefill_case(77, [prefix], [n], H=32, G=8, D=128, bs=16, dtype=torch.bfloat16)
+    whole, whole_lse = gpu_prefill(case)
+    for chunk in (64, 128, 192):
+        pos = prefix
+        while pos < prefix + n:
+            m = min(chunk, prefix + n - pos)
+            sub = wl.PrefillCase(name="sub", q=case.q[pos - prefix:pos - prefix + m],
+                                 cu_q_lens=torch.tensor([0, m], dtype=torch.int32), k_cache=case.k_cache,
+                                 v_cache=case.v_cache, block_table=case.block_table,
+                                 seq_lens=torch.tensor([pos + m], dtype=torch.int32), scale=case.scale)
+            part, part_lse = gpu_prefill(sub, max_seq_len=prefix + n)
+            ref = f64(whole[pos - prefix:pos - prefix + m])
+            assert_parity(part, ref, torch.bfloat16)
+            assert (part_lse - whole_lse[pos - prefix:pos - prefix + m]).abs().max().item() <= 1e-3
+            pos += m
+
+
+def test_block_permutation_is_bitwise_invariant():
+    from helpers import replace_blocks
+    case = wl.make_prefill_case(91, [100, 0, 333], [150, 64, 1], H=32, G=8, D=128, bs=16, dtype=torch.bfloat16,
+                                extra_blocks=10)
+    base, base_lse = gpu_prefill(case)
+    k2, v2, bt2 = replace_blocks(case.k_cache, case.v_cache, case.block_table, case.seq_lens, 3)
+    out, lse = gpu_prefill(case, k_cache=k2, v_cache=v2, block_table=bt2)
+    assert torch.equal(out, base) and torch.equal(lse, base_lse)
+
+
+def test_chunked_prefill_full_size_sampled():
+    """16 chunks of 512 over prefixes U[0, 4096] + 48 decodes: sampled rows (every decode row, chunk rows at
+    tile edges) against the oracle, and every output finite."""
+    case = wl.config4_chunked_prefill()
+    out, lse = gpu_prefill(case)
+    assert pa.metis_read_status() == 0
+    o = f64(out)
+    assert np.isfinite(o).all()
+    cu = case.cu_q_lens.numpy()
+    rng = np.random.default_rng(0)
+    rows = []
+    for s in range(case.S):
+        q_len = int(cu[s + 1] - cu[s])
+        picks = [0, q_len - 1] + ([31, 32, 255, 256] if q_len > 256 else []) + list(rng.integers(0, q_len, 2))
+        for i in sorted(set(picks)):
+            rows.append((int(cu[s]) + i, int(rng.integers(0, case.H))))
+    ref_o, ref_l = oracle.paged_prefill_rows(case.q, case.cu_q_lens, case.k_cache, case.v_cache, case.block_table,
+                                             case.seq_lens, case.scale, rows)
+    got = torch.stack([out[t, h] for t, h in rows])
+    got_l = torch.stack([lse[t, h] for t, h in rows])
+    assert_parity(got, ref_o, torch.bfloat16)
+    assert_lse(got_l, ref_l, torch.bfloat16)
+
+
+def test_bad_block_id_and_q_len_are_flagged():
+    case = wl.make_prefill_case(19, [40, 10], [20, 5], H=8, G=2, D=128, bs=16, dtype=torch.bfloat16)
+    bt = case.block_table.clone()
+    bt[0, 1] = case.num_blocks + 99
+    out, _ = gpu_prefill(case, block_table=bt)
+    assert pa.metis_read_status() & pa.STATUS_BAD_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ref_o, _ = oracle_prefill(case)
+    cu = case.cu_q_lens.numpy()
+    assert_parity(out[cu[1]:], ref_o[cu[1]:], torch.bfloat16)   # the other sequence is untouched
+    # q_len > seq_len: clamped, flagged, never a fault
+    bad = wl.PrefillCase(name="bad", q=case.q, cu_q_lens=case.cu_q_lens, k_cache=case.k_cache,
+                         v_cache=case.v_cache, block_table=case.block_table,
+                         seq_lens=torch.tensor([10, 15], dtype=torch.int32), scale=case.scale)
+    gpu_prefill(bad, max_seq_len=60)
+    assert pa.metis_read_status() & pa.STATUS_BAD_Q_LEN
