@@ -213,6 +213,43 @@ int metis_paged_attn_prefill_chunk(const void* q, const int32_t* cu_q_lens,
 size_t metis_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads, int num_kv_heads);
 
 /*
+ * metis_mla_decode -- multi-head latent attention decode over a paged latent
+ * cache (the MLA kernel of the vllm-metal article, section 3, fed by the block
+ * table and sequence lengths of section 4).
+ *
+ * All heads share one latent cache whose rows are [c_kv (d_latent) | k_pe
+ * (d_rope)]; queries arrive already in latent space.  For head h of sequence s:
+ *   z_t = scale * q[s,h,:] . kv[t, 0:d_latent+d_rope]
+ *   out[s,h,:] = sum_t softmax(z)_t kv[t, 0:d_latent]
+ *
+ *   q          [num_seqs, num_heads, d_latent + d_rope] bf16
+ *   kv_cache   [num_blocks, block_size, d_latent + d_rope] bf16
+ *   block_table, seq_lens   as for metis_paged_attn_decode
+ *   out        [num_seqs, num_heads, d_latent] bf16 (written)
+ *   lse_out    fp32 [num_seqs, num_heads] or NULL
+ *   partition_size  0: one pass per sequence; > 0 (a multiple of 32): tokens
+ *              are split into partitions of that size, computed in parallel and
+ *              merged by log-sum-exp (a sequence with one partition is written
+ *              directly)
+ *   workspace  >= metis_mla_workspace_bytes(...) bytes, 256-byte aligned, no
+ *              initialisation needed
+ *
+ * Supported: d_latent 512, d_rope 64; num_heads a multiple of 128, or a
+ * multiple of 16 below 128; block_size 16, 32 or 64.  Tensor cores: bf16
+ * operands, fp32 accumulation.
+ */
+int metis_mla_decode(const void* q, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens,
+                     void* out, float* lse_out,
+                     int num_seqs, int num_heads, int d_latent, int d_rope,
+                     int block_size, int max_blocks, int num_blocks, float scale,
+                     int partition_size, int max_seq_len,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace metis_mla_decode needs. */
+size_t metis_mla_workspace_bytes(int num_seqs, int num_heads, int max_seq_len, int partition_size);
+
+/*
  * metis_merge_attn_states -- the log-sum-exp merge of split-KV partials:
  *
  *   lse = m + ln sum_p exp(lse_p - m),  m = max_p lse_p

@@ -21,6 +21,8 @@ from ._binding import (  # noqa: F401
     metis_decode_workspace_bytes,
     metis_last_error,
     metis_merge_attn_states,
+    metis_mla_decode,
+    metis_mla_workspace_bytes,
     NOALLOC_SCRATCH_BYTES,
     metis_paged_attn_decode,
     metis_paged_attn_decode_noalloc,

@@ -66,6 +66,8 @@ SIGNATURES = {
     "metis_paged_attn_prefill_chunk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                                             _i, _f, _i, _vp, _sz, _vp]),
     "metis_prefill_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "metis_mla_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
+    "metis_mla_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "metis_merge_attn_states": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "metis_read_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
     "metis_last_error": (ctypes.c_char_p, []),
@@ -320,4 +322,43 @@ def metis_paged_attn_prefill_chunk(q: torch.Tensor, cu_q_lens: torch.Tensor, k_c
         _ptr(q), _ptr(cu_q_lens), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out),
         _ptr(lse_out), S, T, H, G, D, bs, block_table.shape[1], nb, dt, float(scale), int(max_seq_len),
         _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, lse_out
+
+
+def metis_mla_workspace_bytes(num_seqs: int, num_heads: int, max_seq_len: int, partition_size: int) -> int:
+    return int(load_library().metis_mla_workspace_bytes(num_seqs, num_heads, max_seq_len, partition_size))
+
+
+def metis_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                     scale: float, *, d_latent: int = 512, out: Optional[torch.Tensor] = None,
+                     lse_out: Optional[torch.Tensor] = None, partition_size: int = 0,
+                     max_seq_len: Optional[int] = None, workspace: Optional[torch.Tensor] = None, stream=None,
+                     want_lse: bool = False):
+    """MLA decode over a paged latent cache; returns ``(out, lse_out)``."""
+    lib = load_library()
+    _cuda("q", q, dtype=torch.bfloat16, ndim=3)
+    _cuda("kv_cache", kv_cache, dtype=torch.bfloat16, ndim=3)
+    _cuda("block_table", block_table, dtype=torch.int32, ndim=2)
+    _cuda("seq_lens", seq_lens, dtype=torch.int32, ndim=1)
+    S, H, dq = q.shape
+    nb, bs, dk = kv_cache.shape
+    if dk != dq or block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((S, H, d_latent), dtype=q.dtype, device=q.device)
+    _cuda("out", out, dtype=q.dtype, ndim=3)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((S, H), dtype=torch.float32, device=q.device)
+    if lse_out is not None:
+        _cuda("lse_out", lse_out, dtype=torch.float32, ndim=2)
+    if max_seq_len is None:
+        max_seq_len = max(1, int(seq_lens.max().item())) if S else 1
+    need = metis_mla_workspace_bytes(S, H, max_seq_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.metis_mla_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out),
+                                _ptr(lse_out), S, H, d_latent, dq - d_latent, bs, block_table.shape[1], nb,
+                                float(scale), int(partition_size), int(max_seq_len), _ptr(workspace), ws_bytes,
+                                _stream(stream)))
     return out, lse_out

@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
                                                               const float* __restrict__ part_lse,
                                                               const int32_t* __restrict__ seq_lens, int P,
                                                               OutT* __restrict__ out, float* __restrict__ lse_out,
-                                                              int H, int D, int max_parts) {
+                                                              int H, int D, int max_parts, int skip_single) {
   constexpr int NWARP = kMergeThreads / 32;
   __shared__ float red[NWARP];
   __shared__ float4 acc_s[NWARP][kMergeMaxD / 4];
@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = seq_lens[s];
   const int n = L > 0 ? min((L + P - 1) / P, max_parts) : 0;
+  if (skip_single && n <= 1) return;  // written directly by the producing kernel
   const float* lrow = part_lse + sh * max_parts;
 
   // max of the partition lse values (natural log)
@@ -537,6 +538,68 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   if (threadIdx.x == 0 && lse_out) lse_out[sh] = empty ? -INFINITY : M + log2f(W) * kLn2;
 }
 
+// One warp per (sequence, head) when there are few partitions: lanes share the
+// lse reductions and own float4 columns lane, lane + 32, ...
+template <typename OutT>
+__global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* __restrict__ part_out,
+                                                                   const float* __restrict__ part_lse,
+                                                                   const int32_t* __restrict__ seq_lens, int P,
+                                                                   OutT* __restrict__ out,
+                                                                   float* __restrict__ lse_out, int S, int H, int D,
+                                                                   int max_parts, int skip_single) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t sh = (size_t)blockIdx.x * (kMergeThreads / 32) + warp;
+  if (sh >= (size_t)S * H) return;
+  const int s = (int)(sh / H);
+  const int L = seq_lens[s];
+  const int n = L > 0 ? min((L + P - 1) / P, max_parts) : 0;
+  if (skip_single && n <= 1) return;
+  const float* lrow = part_lse + sh * max_parts;
+  float M = -INFINITY;
+  for (int i = lane; i < n; i += 32) M = fmaxf(M, lrow[i]);
+  M = warp_max_xor(M, 1);
+  const bool empty = !(M > -INFINITY);
+  const float M2 = M * kLog2e;
+  float W = 0.f;
+  if (!empty)
+    for (int i = lane; i < n; i += 32) {
+      const float x = lrow[i];
+      if (x > -INFINITY) W += exp2_approx(fmaf(x, kLog2e, -M2));
+    }
+  W = warp_sum_xor(W, 1);
+  const int nq = D / 4;
+  float4 acc[kMergeMaxD / 128];
+#pragma unroll
+  for (int j = 0; j < kMergeMaxD / 128; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!empty) {
+    const float4* prow = reinterpret_cast<const float4*>(part_out + sh * max_parts * D);
+    for (int i = 0; i < n; ++i) {
+      const float x = lrow[i];
+      if (!(x > -INFINITY)) continue;
+      const float w = exp2_approx(fmaf(x, kLog2e, -M2));
+#pragma unroll
+      for (int j = 0; j < kMergeMaxD / 128; ++j) {
+        const int c = lane + 32 * j;
+        if (c < nq) {
+          const float4 v = __ldg(prow + (size_t)i * nq + c);
+          acc[j].x = fmaf(w, v.x, acc[j].x);
+          acc[j].y = fmaf(w, v.y, acc[j].y);
+          acc[j].z = fmaf(w, v.z, acc[j].z);
+          acc[j].w = fmaf(w, v.w, acc[j].w);
+        }
+      }
+    }
+  }
+  const float inv = empty ? 0.f : 1.0f / W;
+#pragma unroll
+  for (int j = 0; j < kMergeMaxD / 128; ++j) {
+    const int c = lane + 32 * j;
+    if (c < nq) store4<OutT>(out + sh * D + (size_t)c * 4, acc[j].x * inv, acc[j].y * inv, acc[j].z * inv,
+                             acc[j].w * inv);
+  }
+  if (lane == 0 && lse_out) lse_out[sh] = empty ? -INFINITY : M + log2f(W) * kLn2;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -553,17 +616,39 @@ int decode_status(uint32_t* bits, int clear) {
   return METIS_OK;
 }
 
+// Few partitions: a warp per (sequence, head); many: a CTA per (sequence, head)
+// whose warps split the partitions.
+int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,
+                    float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int skip_single,
+                    cudaStream_t st) {
+  const size_t pairs = (size_t)S * H;
+  if (max_parts <= 16) {
+    const unsigned grid = (unsigned)((pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
+    if (out_dtype == METIS_BF16)
+      merge_warp_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(
+          part_out, part_lse, seq_lens, P, reinterpret_cast<__nv_bfloat16*>(out), lse_out, S, H, D, max_parts,
+          skip_single);
+    else
+      merge_warp_kernel<float><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
+                                                                reinterpret_cast<float*>(out), lse_out, S, H, D,
+                                                                max_parts, skip_single);
+  } else {
+    const unsigned grid = (unsigned)pairs;
+    if (out_dtype == METIS_BF16)
+      merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
+                                                                   reinterpret_cast<__nv_bfloat16*>(out), lse_out, H,
+                                                                   D, max_parts, skip_single);
+    else
+      merge_kernel<float><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
+                                                           reinterpret_cast<float*>(out), lse_out, H, D, max_parts,
+                                                           skip_single);
+  }
+  return check_launch("merge kernel launch");
+}
+
 static int launch_merge(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,
                         float* lse_out, int S, int H, int D, int max_parts, int out_dtype, cudaStream_t st) {
-  const unsigned grid = (unsigned)((size_t)S * H);
-  if (out_dtype == METIS_BF16)
-    merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
-                                                                 reinterpret_cast<__nv_bfloat16*>(out), lse_out, H,
-                                                                 D, max_parts);
-  else
-    merge_kernel<float><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
-                                                         reinterpret_cast<float*>(out), lse_out, H, D, max_parts);
-  return check_launch("merge_kernel launch");
+  return launch_merge_ex(part_out, part_lse, seq_lens, P, out, lse_out, S, H, D, max_parts, out_dtype, 0, st);
 }
 
 static size_t split_parts(int max_seq_len, int partition_size) {

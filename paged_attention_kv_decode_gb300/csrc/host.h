@@ -29,8 +29,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Log-sum-exp merge of split partials [S, H, max_parts, D] (decode.cu); with
+// skip_single, sequences with at most one partition are left untouched.
+int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,
+                    float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int skip_single,
+                    cudaStream_t st);
+
 // Per-translation-unit device status words.
 int decode_status(uint32_t* bits, int clear);
 int prefill_status(uint32_t* bits, int clear);
+int mla_status(uint32_t* bits, int clear);
 
 }  // namespace metis

@@ -40,9 +40,9 @@ namespace metis {
 __device__ unsigned int g_status_prefill = 0;
 
 constexpr int kPfThreads = 192;   // 4 softmax warps + TMA warp + MMA warp
-constexpr int kKvTile = 128;      // tokens per K/V tile
+constexpr int kKvTile = 64;       // tokens per K/V tile
 constexpr int kRows = 128;        // query rows per tile
-constexpr int kTmemCols = 512;    // S0 | S1 | O
+constexpr int kTmemCols = 256;    // S0 | S1 | O: two CTAs share an SM's 512 columns
 constexpr int kSortMax = 2048;    // schedule: heaviest-first sort up to this many tiles
 
 struct PrefillParams {
@@ -57,19 +57,24 @@ struct PrefillParams {
   float scale_log2;
 };
 
+// Shared-memory layout (all tiles 128-byte swizzled, [64-column half][row][128 B]).
 template <int D>
 struct PfShape {
   static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = kRows * 128;               // 128 rows x 64 bf16
-  static constexpr int kTileBytes = kHalves * kHalfBytes;      // a 128 x D bf16 tile
+  static constexpr int kQHalf = kRows * 128;                   // 128 query rows x 64 bf16
+  static constexpr int kQBytes = kHalves * kQHalf;
+  static constexpr int kKvHalf = kKvTile * 128;                // 64 tokens x 64 bf16
+  static constexpr int kKvBytes = kHalves * kKvHalf;
+  static constexpr int kPBytes = kRows * kKvTile * 2;          // P: 128 rows x 64 tokens (one half)
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;                   // 2 stages
-  static constexpr int kV = kK + 2 * kTileBytes;               // 2 stages
-  static constexpr int kP = kV + 2 * kTileBytes;               // 128 x 128 bf16, 2 halves
-  static constexpr int kBar = kP + 2 * kHalfBytes;
-  // + barriers and alignment slack; at least 120 KB so that one CTA (which takes all
-  // 512 TMEM columns) is resident per SM
-  static constexpr int kSmem = (kBar + 256 + 1024) > 120 * 1024 ? (kBar + 256 + 1024) : 120 * 1024;
+  static constexpr int kK = kQ + kQBytes;                      // 2 stages
+  static constexpr int kV = kK + 2 * kKvBytes;                 // 2 stages
+  static constexpr int kP = kV + 2 * kKvBytes;
+  static constexpr int kTiles = kP + kPBytes;                  // 112 KB at head_dim 128
+  // + 1 KB: the barriers live in the alignment slack (below the aligned base when
+  // it is at least 256 B, else just past the tiles).  At least 80 KB, so that at
+  // most two CTAs -- 2 x 256 TMEM columns -- are resident per SM.
+  static constexpr int kSmem = (kTiles + 1024) > 80 * 1024 ? (kTiles + 1024) : 80 * 1024;
 };
 
 // Effective (sequence length, query count) after clamping to what can be read.
@@ -149,19 +154,20 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
 // main kernel
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+__global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                        const __grid_constant__ CUtensorMap tmK,
                                                                        const __grid_constant__ CUtensorMap tmV,
                                                                        const PrefillParams p) {
   using Sh = PfShape<D>;
   constexpr int HALVES = Sh::kHalves;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t slack = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + slack;
   uint8_t* sQ = smem + Sh::kQ;
   uint8_t* sK = smem + Sh::kK;
   uint8_t* sV = smem + Sh::kV;
   uint8_t* sP = smem + Sh::kP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slack >= 256 ? smem - 256 : smem + Sh::kTiles);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;   // [2]
   uint64_t* k_empty = bars + 3;  // [2]
@@ -229,11 +235,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, Sh::kTileBytes);
+      mbar_arrive_expect_tx(q_full, Sh::kQBytes);
       const uint64_t pol = l2_policy_evict_first();
       for (int hh = 0; hh < p.r; ++hh)
         for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(sQ + h * Sh::kHalfBytes + hh * p.Tq * 128, &tmQ, q_full, h * 64, g * p.r + hh, q0 + qi0, pol);
+          tma_load_3d(sQ + h * Sh::kQHalf + hh * p.Tq * 128, &tmQ, q_full, h * 64, g * p.r + hh, q0 + qi0, pol);
     }
     const int npg = kKvTile / p.bs;  // pages per K/V tile
     const uint64_t pol = l2_policy_evict_last();
@@ -252,14 +258,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       __syncwarp();
       if (live)
         for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(sK + st * Sh::kTileBytes + h * Sh::kHalfBytes + lane * p.bs * 128, &tmK, &k_full[st], h * 64, g,
+          tma_load_3d(sK + st * Sh::kKvBytes + h * Sh::kKvHalf + lane * p.bs * 128, &tmK, &k_full[st], h * 64, g,
                       rowc, pol);
       if (j >= 2 && !wait_all(&v_empty[st], ((j >> 1) - 1) & 1)) break;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
       __syncwarp();
       if (live)
         for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(sV + st * Sh::kTileBytes + h * Sh::kHalfBytes + lane * p.bs * 128, &tmV, &v_full[st], h * 64, g,
+          tma_load_3d(sV + st * Sh::kKvBytes + h * Sh::kKvHalf + lane * p.bs * 128, &tmV, &v_full[st], h * 64, g,
                       rowc, pol);
     }
     if (*abort_flag) {
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     // ------------------------------------------------------------ UMMA issuer
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kRows, kKvTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kRows, D, false, true);
-    const uint32_t o_tmem = tmem + 256;
+    const uint32_t o_tmem = tmem + 2 * kKvTile;
     bool issued = false;
     auto do_pv = [&](int i) -> bool {
       const int st = i & 1;
@@ -284,10 +290,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       if (tok0 + kKvTile > L) {
         // rows past the sequence end may hold anything (NaN included): zero them so that P = 0 stays 0
         const int first = L - tok0;
-        uint8_t* vb = sV + st * Sh::kTileBytes;
+        uint8_t* vb = sV + st * Sh::kKvBytes;
         for (int row = first + lane; row < kKvTile; row += 32)
           for (int h = 0; h < HALVES; ++h) {
-            uint4* d = reinterpret_cast<uint4*>(vb + h * Sh::kHalfBytes + row * 128);
+            uint4* d = reinterpret_cast<uint4*>(vb + h * Sh::kKvHalf + row * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
           }
@@ -296,11 +302,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       }
       if (lane == 0) {
         const uint32_t pbase = smem_u32(sP);
-        const uint32_t vbase = smem_u32(sV + st * Sh::kTileBytes);
+        const uint32_t vbase = smem_u32(sV + st * Sh::kKvBytes);
 #pragma unroll
         for (int kk = 0; kk < kKvTile / 16; ++kk) {
-          const uint64_t a = umma_desc_sw128(pbase + (kk >> 2) * Sh::kHalfBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = umma_desc_sw128(vbase + kk * 2048, Sh::kHalfBytes, 1024);
+          const uint64_t a = umma_desc_sw128(pbase + kk * 32, 16, 1024);             // P: one 64-token half
+          const uint64_t b = umma_desc_sw128(vbase + kk * 2048, Sh::kKvHalf, 1024);  // V: MN-major
           umma_bf16(o_tmem, a, b, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(pv_done);
@@ -319,12 +325,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       tc_fence_after_sync();
       if (lane == 0) {
         const uint32_t qbase = smem_u32(sQ);
-        const uint32_t kbase = smem_u32(sK + st * Sh::kTileBytes);
+        const uint32_t kbase = smem_u32(sK + st * Sh::kKvBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Sh::kHalfBytes + (kk & 3) * 32;
-          umma_bf16(tmem + (j & 1) * 128, umma_desc_sw128(qbase + off, 16, 1024),
-                    umma_desc_sw128(kbase + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+          const uint32_t within = (kk & 3) * 32;
+          umma_bf16(tmem + (j & 1) * kKvTile, umma_desc_sw128(qbase + (kk >> 2) * Sh::kQHalf + within, 16, 1024),
+                    umma_desc_sw128(kbase + (kk >> 2) * Sh::kKvHalf + within, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[j & 1]);
         umma_commit(&k_empty[st]);
@@ -348,8 +354,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     const bool row_valid = qi < q_len;
     const int p_row = row_valid ? (L - q_len + qi) : p_max;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t o_tmem = lane_base + 256;
+    const uint32_t o_tmem = lane_base + 2 * kKvTile;
     const float sl2 = p.scale_log2;
+    const float sgn = sl2 < 0.f ? -1.f : 1.f;   // max of sl2 * s = |sl2| * max(sgn * s)
+    const float asl2 = fabsf(sl2);
     uint8_t* prow = sP + row * 128;
     const int sw = row & 7;
     float m_run = -INFINITY, l_run = 0.f;
@@ -362,25 +370,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       tc_fence_after_sync();
       uint32_t sv[kKvTile];
 #pragma unroll
-      for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(lane_base + (j & 1) * 128 + c * 32, sv + c * 32);
+      for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(lane_base + (j & 1) * kKvTile + c * 32, sv + c * 32);
       tmem_ld_wait();
       float* sc = reinterpret_cast<float*>(sv);
       const int tok0 = j * kKvTile;
-      float mx = -INFINITY;
-      if (tok0 + kKvTile - 1 > p_min) {
+      // Visible keys of this row in this tile form a prefix: t <= p_row.  Scores stay raw
+      // (times the sign of the scale); |scale| * log2(e) is folded into the max and into
+      // one FMA per exponent.
+      const int vis = tok0 + kKvTile - 1 > p_min ? min(max(p_row - tok0 + 1, 0), kKvTile) : kKvTile;
+      const bool lean = vis == kKvTile && sgn > 0.f;   // the common case: no mask, positive scale
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (lean) {
 #pragma unroll
-        for (int c = 0; c < kKvTile; ++c) {
-          sc[c] = (tok0 + c <= p_row) ? sc[c] * sl2 : -INFINITY;
-          mx = fmaxf(mx, sc[c]);
+        for (int c = 0; c < kKvTile; c += 2) {
+          mx0 = fmaxf(mx0, sc[c]);
+          mx1 = fmaxf(mx1, sc[c + 1]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kKvTile; ++c) {
-          sc[c] *= sl2;
-          mx = fmaxf(mx, sc[c]);
+        for (int c = 0; c < kKvTile; c += 2) {
+          mx0 = fmaxf(mx0, c < vis ? sc[c] * sgn : -INFINITY);
+          mx1 = fmaxf(mx1, c + 1 < vis ? sc[c + 1] * sgn : -INFINITY);
         }
       }
-      const float m_new = fmaxf(m_run, mx);
+      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * asl2);
       const bool grow = m_new > m_run + 8.0f;   // rescale only when the max grew past 2^8
       float alpha = 1.f;
       if (grow) {
@@ -408,23 +421,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         }
       }
       l_run *= alpha;
-      float lsum = 0.f;
+      float lsum0 = 0.f, lsum1 = 0.f;
+      const float neg_m = -m_run;
 #pragma unroll
       for (int c8 = 0; c8 < kKvTile / 8; ++c8) {
         float e[8];
+        if (lean) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          e[i] = exp2_approx(sc[c8 * 8 + i] - m_run);
-          lsum += e[i];
+          for (int i = 0; i < 8; ++i) e[i] = exp2_approx(fmaf(sc[c8 * 8 + i], asl2, neg_m));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            e[i] = c8 * 8 + i < vis ? exp2_approx(fmaf(sc[c8 * 8 + i] * sgn, asl2, neg_m)) : 0.f;
         }
+        lsum0 += (e[0] + e[1]) + (e[2] + e[3]);
+        lsum1 += (e[4] + e[5]) + (e[6] + e[7]);
         uint4 v;
         v.x = pack_bf16x2(e[0], e[1]);
         v.y = pack_bf16x2(e[2], e[3]);
         v.z = pack_bf16x2(e[4], e[5]);
         v.w = pack_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + (c8 >> 3) * PfShape<D>::kHalfBytes + (((c8 & 7) ^ sw) << 4)) = v;
+        *reinterpret_cast<uint4*>(prow + (((c8 & 7) ^ sw) << 4)) = v;
       }
-      l_run += lsum;
+      l_run += lsum0 + lsum1;
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(p_full);

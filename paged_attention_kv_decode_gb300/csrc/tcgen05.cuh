@@ -55,6 +55,19 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// K-major operand with 64-byte swizzle: rows of 32 bf16 (64 B), 8-row groups
+// `sbo` bytes apart; the 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+// Atoms start on 512-byte boundaries.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;  // leading byte offset: unused for swizzled K-major
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and an fp32 accumulator.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |

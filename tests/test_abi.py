@@ -164,3 +164,25 @@ def test_prefill_workspace_bytes(lib):
     # 4 heads per group -> 32-token query tiles: ceil(100 / 32) + 4 sequences = 8 tiles of 16 bytes + header
     assert pa.metis_prefill_workspace_bytes(4, 100, 32, 8) == 256 + 8 * 16
     assert pa.metis_prefill_workspace_bytes(0, 100, 32, 8) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(kv=None), -1), (dict(dl=256), -3), (dict(dr=32), -3), (dict(H=100), -3),
+    (dict(bs=8), -3), (dict(P=48), -2), (dict(q=FAKE + 4), -4), (dict(ws=None), -5), (dict(ws_bytes=8), -5),
+    (dict(S=-2), -2),
+])
+def test_mla_rejects(lib, kw, code):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, out=FAKE, lse=None, S=4, H=128, dl=512, dr=64, bs=64,
+             max_blocks=8, num_blocks=64, scale=0.07, P=256, max_len=512, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    rc = lib.metis_mla_decode(vp(a["q"]), vp(a["kv"]), vp(a["bt"]), vp(a["sl"]), vp(a["out"]), vp(a["lse"]), a["S"],
+                              a["H"], a["dl"], a["dr"], a["bs"], a["max_blocks"], a["num_blocks"], a["scale"], a["P"],
+                              a["max_len"], vp(a["ws"]), a["ws_bytes"], None)
+    assert rc == code
+
+
+def test_mla_workspace_bytes(lib):
+    assert pa.metis_mla_workspace_bytes(4, 128, 512, 0) > 0
+    n = pa.metis_mla_workspace_bytes(4, 128, 512, 256)       # 2 partitions of fp32 partials
+    assert n >= 4 * 128 * 2 * 512 * 4

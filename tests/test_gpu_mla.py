@@ -1,0 +1,118 @@
+"""GPU parity of MLA decode (128 heads over a 512 + 64 latent cache) against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_attention_kv_decode_gb300 as pa
+from paged_attention_kv_decode_gb300 import workloads as wl
+from helpers import assert_lse, assert_parity, dev, f64, replace_blocks
+
+pytestmark = pytest.mark.gpu
+
+# the partition size bench.py uses for the MLA workload
+BENCH_MLA_PARTITION = 1024
+
+
+@pytest.fixture(autouse=True)
+def _clear_status():
+    if torch.cuda.is_available():
+        pa.metis_read_status(clear=True)
+    yield
+
+
+def oracle_mla(case):
+    return oracle.mla_decode(case.q, case.kv_cache, case.block_table, case.seq_lens, case.scale,
+                             d_latent=case.d_latent)
+
+
+def gpu_mla(case, partition_size=0, kv_cache=None, block_table=None, max_seq_len=None):
+    out, lse = pa.metis_mla_decode(dev(case.q), dev(case.kv_cache if kv_cache is None else kv_cache),
+                                   dev(case.block_table if block_table is None else block_table),
+                                   dev(case.seq_lens), case.scale, partition_size=partition_size,
+                                   max_seq_len=max_seq_len or max(1, case.max_seq_len), want_lse=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check(case, partition_size):
+    ref_o, ref_l = oracle_mla(case)
+    out, lse = gpu_mla(case, partition_size)
+    assert_parity(out, ref_o, torch.bfloat16)
+    assert_lse(lse, ref_l, torch.bfloat16)
+    assert pa.metis_read_status() == 0
+
+
+EDGE = [1, 31, 32, 33, 63, 64, 65, 100, 1000, 2049]
+
+
+@pytest.mark.parametrize("partition_size", [0, 32, 64, 256, 2048])
+def test_edge_lengths(partition_size):
+    case = wl.make_mla_case(61, EDGE, H=128, bs=64, extra_blocks=4, poison=True)
+    check(case, partition_size)
+
+
+@pytest.mark.parametrize("bs,H", [(16, 128), (32, 128), (64, 64), (64, 16), (16, 256)])
+def test_shapes(bs, H):
+    case = wl.make_mla_case(70 + bs + H, [1, 17, 64, 333, 700], H=H, bs=bs, extra_blocks=3, poison=True)
+    check(case, 0)
+    check(case, 128)
+
+
+def test_mla_recipe_small():
+    case = wl.config5_mla_decode(poison=True, num_seqs=16, median=120, cap=900, extra_blocks=5)
+    check(case, 0)
+    check(case, 256)
+
+
+def test_block_permutation_is_bitwise_invariant():
+    case = wl.make_mla_case(83, [5, 300, 1200], H=128, bs=64, extra_blocks=9)
+    base, base_lse = gpu_mla(case, 256)
+    nb = case.num_blocks
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(nb).astype(np.int64))
+    kv2 = torch.empty_like(case.kv_cache)
+    kv2[perm] = case.kv_cache
+    bt = case.block_table.clone().to(torch.int64)
+    used = bt >= 0
+    bt[used] = perm[bt[used]]
+    out, lse = gpu_mla(case, 256, kv_cache=kv2, block_table=bt.to(torch.int32))
+    assert torch.equal(out, base) and torch.equal(lse, base_lse)
+
+
+def test_empty_sequence():
+    case = wl.make_mla_case(84, [0, 70, 0], H=128, bs=64, extra_blocks=2)
+    for P in (0, 64):
+        out, lse = gpu_mla(case, P, max_seq_len=70)
+        assert (out[0].float() == 0).all() and (out[2].float() == 0).all()
+        assert torch.isinf(lse[0]).all() and torch.isinf(lse[2]).all()
+        ref_o, _ = oracle_mla(case)
+        assert_parity(out, ref_o, torch.bfloat16)
+
+
+def test_mla_full_size_sampled():
+    """128 seqs, lognormal lengths (median 1024, cap 8192), 128 heads: 12 whole sequences vs the oracle."""
+    case = wl.config5_mla_decode()
+    out, lse = gpu_mla(case, BENCH_MLA_PARTITION)
+    assert pa.metis_read_status() == 0
+    assert np.isfinite(f64(out)).all()
+    lens = case.seq_lens.numpy()
+    order = np.argsort(lens)
+    pick = sorted(set(list(order[:4]) + list(order[-4:]) + list(order[len(order) // 2 - 2:len(order) // 2 + 2])))
+    for s in pick:
+        sub = wl.MLACase(name="sub", q=case.q[s:s + 1], kv_cache=case.kv_cache, block_table=case.block_table[s:s + 1],
+                         seq_lens=case.seq_lens[s:s + 1], scale=case.scale)
+        ref_o, ref_l = oracle_mla(sub)
+        assert_parity(out[s:s + 1], ref_o, torch.bfloat16)
+        assert_lse(lse[s:s + 1], ref_l, torch.bfloat16)
+
+
+def test_bad_block_id_is_flagged():
+    case = wl.make_mla_case(85, [130, 90], H=128, bs=64)
+    bt = case.block_table.clone()
+    bt[0, 1] = case.num_blocks + 7
+    out, _ = gpu_mla(case, 0, block_table=bt)
+    assert pa.metis_read_status() & pa.STATUS_BAD_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ref_o, _ = oracle_mla(case)
+    assert_parity(out[1:], ref_o[1:], torch.bfloat16)
