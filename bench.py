@@ -12,6 +12,11 @@ timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The line also carries ``workloads``: the tiny fp32 decode, the long-context
+split-KV decode (GB/s), the chunked prefill mixed with decodes (TFLOP/s against
+the measured bf16 peak) and the MLA decode (TFLOP/s and GB/s), each timed the
+same way as one call of its entry point.
+
 ``value`` is decode KV GB/s: the algorithmic bytes of a step (every cached
 token's K and V row for its KV head, the queries, outputs, block-table
 entries and lengths; partials are overhead and not counted) divided by the
@@ -45,7 +50,9 @@ METRIC = "decode KV GB/s (% of HBM peak) and tokens/s; prefill TFLOP/s, 1 GB300"
 WORKLOAD = ("batched paged decode, bf16 KV: 64 seqs, seq_lens U[512,4096], 32 q / 8 kv heads, head_dim 128, "
             "block_size 16, block_table a random permutation of the pool")
 PARTITION = 1024
+MLA_PARTITION = 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TC_TFLOPS = (1900.0, 1700.0)
 
 
 def log(*a):
@@ -70,6 +77,17 @@ def load_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_tc_peaks():
+    """bf16 dense TFLOP/s: (burst, sustained)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return (float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"])), "measured"
+    except Exception:
+        return FALLBACK_TC_TFLOPS, "fallback"
 
 
 def source_hash() -> str:
@@ -390,10 +408,109 @@ def run_ours(args, world, rank, local):
         "device_status": status,
         "clocks": sampler.summary(),
     }
+    if args.workloads:
+        (tcb, tcs), tc_src = load_tc_peaks()
+        names = [w.strip() for w in args.workloads.split(",") if w.strip()]
+        line["workloads"] = other_workloads(names, args.workload_reps, dev, flush, stream, peak, (tcb, tcs))
+        line["workloads"]["peaks"] = {"hbm_GB_s": peak, "bf16_TFLOP_s_burst": tcb, "bf16_TFLOP_s_sustained": tcs,
+                                      "source": tc_src}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case)
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# the other workloads: timed the same way (events, untimed L2 flush between reps)
+# ---------------------------------------------------------------------------
+
+def _time_calls(call, reps, flush, stream):
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return float(np.median(ts)), float(np.min(ts))
+
+
+def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
+    import paged_attention_kv_decode_gb300 as pa
+    from paged_attention_kv_decode_gb300 import workloads as wl
+    res = {}
+    tc_burst, tc_sus = peaks_tc
+    if "c1" in names:
+        c = wl.config1_tiny_decode()
+        t = [x.to(dev) for x in (c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
+        out = torch.empty_like(t[0])
+        med, mn = _time_calls(lambda: pa.metis_paged_attn_decode(*t, c.scale, out=out, max_seq_len=c.max_seq_len,
+                                                                  stream=stream), reps, flush, stream)
+        nb = decode_algorithmic_bytes(c)
+        res["tiny_decode_fp32"] = {"ms": med, "GB_s": nb / med / 1e6, "kv_bytes": nb,
+                                   "note": "about 67 KB of KV: launch-latency bound"}
+    if "c3" in names:
+        c = wl.config3_long_split_decode()
+        t = [x.to(dev) for x in (c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
+        out = torch.empty_like(t[0])
+        ws = torch.empty(pa.metis_decode_workspace_bytes(c.S, c.H, c.D, c.max_seq_len, c.partition_size),
+                         dtype=torch.uint8, device=dev)
+        med, mn = _time_calls(lambda: pa.metis_paged_attn_decode(*t, c.scale, out=out, partition_size=c.partition_size,
+                                                                  max_seq_len=c.max_seq_len, workspace=ws,
+                                                                  stream=stream), reps, flush, stream)
+        nb = decode_algorithmic_bytes(c)
+        res["long_split_decode"] = {"ms": med, "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm,
+                                    "kv_bytes": nb, "partition_size": c.partition_size,
+                                    "tokens_per_s": c.S / (med * 1e-3)}
+        del t, out, ws, c
+        torch.cuda.empty_cache()
+    if "c4" in names:
+        c = wl.config4_chunked_prefill()
+        t = [x.to(dev) for x in (c.q, c.cu_q_lens, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
+        out = torch.empty_like(t[0])
+        ws = torch.empty(pa.metis_prefill_workspace_bytes(c.S, c.T, c.H, c.G), dtype=torch.uint8, device=dev)
+        med, mn = _time_calls(lambda: pa.metis_paged_attn_prefill_chunk(*t, c.scale, out=out, max_seq_len=c.max_seq_len,
+                                                                        workspace=ws, stream=stream), reps, flush,
+                              stream)
+        cu = c.cu_q_lens.numpy()
+        lens = c.seq_lens.numpy()
+        flops = 0
+        for si in range(c.S):
+            ql = int(cu[si + 1] - cu[si])
+            flops += int(((lens[si] - ql) + np.arange(ql) + 1).sum()) * c.H * 4 * c.D
+        tf = flops / med / 1e9
+        res["chunked_prefill"] = {"ms": med, "TFLOP_s": tf, "tensor_frac_burst": tf / tc_burst,
+                                  "tensor_frac_sustained": tf / tc_sus, "flops": flops, "tokens": c.T,
+                                  "tokens_per_s": c.T / (med * 1e-3),
+                                  "note": "one call: 16 chunks of 512 over cached prefixes + 48 single-token decodes"}
+        del t, out, ws, c
+        torch.cuda.empty_cache()
+    if "c5" in names:
+        c = wl.config5_mla_decode()
+        t = [x.to(dev) for x in (c.q, c.kv_cache, c.block_table, c.seq_lens)]
+        out = torch.empty((c.S, c.H, c.d_latent), dtype=torch.bfloat16, device=dev)
+        P = MLA_PARTITION
+        ws = torch.empty(pa.metis_mla_workspace_bytes(c.S, c.H, c.max_seq_len, P), dtype=torch.uint8, device=dev)
+        med, mn = _time_calls(lambda: pa.metis_mla_decode(*t, c.scale, out=out, partition_size=P,
+                                                          max_seq_len=c.max_seq_len, workspace=ws, stream=stream),
+                              reps, flush, stream)
+        tok = int(c.seq_lens.sum())
+        flops = tok * c.H * 2 * (576 + 512)
+        nb = tok * 576 * 2 + c.S * c.H * (576 + 512) * 2 + int(sum(-(-int(L) // c.bs) for L in c.seq_lens)) * 4
+        tf = flops / med / 1e9
+        res["mla_decode"] = {"ms": med, "TFLOP_s": tf, "tensor_frac_burst": tf / tc_burst,
+                             "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm, "flops": flops,
+                             "bytes": nb, "tokens": tok, "partition_size": P,
+                             "tokens_per_s": c.S / (med * 1e-3)}
+        del t, out, ws, c
+        torch.cuda.empty_cache()
+    return res
 
 
 def main():
@@ -404,6 +521,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=PARTITION)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default="c1,c3,c4,c5",
+                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5; empty: none)")
+    ap.add_argument("--workload-reps", type=int, default=20)
     ap.add_argument("--ramp-steps", type=int, default=None,
                     help="untimed steps before warm-up (default: about one second of steps)")
     args = ap.parse_args()
