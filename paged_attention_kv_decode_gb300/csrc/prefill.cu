@@ -10,22 +10,32 @@
 // prefix plus a causal mask inside the chunk).  Single-token decodes are the
 // q_len = 1 case and run through the same tiles.
 //
-// Tiling.  One CTA computes a 128-row query tile of one KV head's group: the
-// r = H/G query heads of the group times 128/r consecutive query tokens
-// (GQA packing, so every K/V tile is read once for the whole group), against
-// 128-token K/V tiles gathered page by page with TMA (128-byte swizzle).
+// Tiling.  A query tile is 128 rows of one KV head's group: the r = H/G query
+// heads times 128/r consecutive query tokens (GQA packing).  One CTA per SM
+// computes TWO consecutive query tiles of the same sequence and group against
+// each 128-token K/V tile, so every K/V byte gathered (page by page, with TMA,
+// 128-byte swizzle) feeds 256 query rows.
 //
-//   warp 4       TMA producer: Q tile once, then K and V tiles into 2-stage rings
-//   warp 5       allocates TMEM; one lane issues the UMMAs:
-//                  S_j = Q K_j^T   (M 128, N 128, K = head_dim)  -> TMEM, double-buffered
-//                  O  += P_j V_j   (M 128, N head_dim, K 128)     -> TMEM
-//   warps 0..3   softmax, one TMEM lane (= one query row) per thread: mask,
-//                running max in log2 units, rescale O in TMEM only when the
-//                max grows by more than 2^8, P = exp2(S - m) as bf16 into a
-//                swizzled shared-memory tile for the PV UMMA; epilogue O / l.
+//   warps 0..3   softmax of query tile 0, one row (TMEM lane) per thread
+//   warps 4..7   softmax of query tile 1
+//   warps 8..11  TMA producers: both query tiles once, then K tiles (warps 8, 9)
+//                and V tiles (warps 10, 11) into 2-stage rings, each tile's pages
+//                split between two warps (16-token pages make many small boxes,
+//                and one warp alone cannot issue them fast enough)
+//   warp 12      allocates TMEM (S0 | S1 | O0 | O1, 512 columns); one lane
+//                issues the UMMAs in the order
+//                  PV0_j, QK0_{j+1}, PV1_j, QK1_{j+1}
+//                so that while one softmax group works the tensor pipe runs the
+//                other group's products (ping-pong).
+//                  S_w = Q_w K_j^T  (M 128, N 128, K = head_dim)
+//                  O_w += P_w V_j   (M 128, N head_dim, K 128; P_w read from TMEM)
+// Softmax: running max in log2 units, P = exp2(S - m) written back as bf16
+// pairs over its own S columns; O is rescaled in TMEM only when the max grows
+// by more than 2^8.  Because QK_w_{j+1} is issued after PV_w_j, "S_w_j landed"
+// already implies "PV_w_{j-1} finished", so the rescale never waits.
 //
-// A small schedule kernel first lists the (sequence, query tile) pairs with
-// work, heaviest first, so the main grid has no idle CTAs.
+// A small schedule kernel first lists the (sequence, query-tile pair) items
+// heaviest first, so the grid has no idle CTAs.
 #include <math.h>
 
 #include <algorithm>
@@ -39,11 +49,13 @@ namespace metis {
 
 __device__ unsigned int g_status_prefill = 0;
 
-constexpr int kPfThreads = 192;   // 4 softmax warps + TMA warp + MMA warp
-constexpr int kKvTile = 64;       // tokens per K/V tile
+constexpr int kPfThreads = 416;   // 2 softmax groups + 4 TMA warps + MMA warp
+constexpr int kMmaWarp = 12;
+constexpr int kKStages = 3;       // K ring depth (V ring: 2)
+constexpr int kKvTile = 128;      // tokens per K/V tile
 constexpr int kRows = 128;        // query rows per tile
-constexpr int kTmemCols = 256;    // S0 | S1 | O: two CTAs share an SM's 512 columns
-constexpr int kSortMax = 2048;    // schedule: heaviest-first sort up to this many tiles
+constexpr int kTmemCols = 512;    // S0 | S1 | O0 | O1
+constexpr int kSortMax = 2048;    // schedule: heaviest-first sort up to this many items
 
 struct PrefillParams {
   const int32_t* cu_q_lens;
@@ -62,19 +74,17 @@ template <int D>
 struct PfShape {
   static constexpr int kHalves = D / 64;
   static constexpr int kQHalf = kRows * 128;                   // 128 query rows x 64 bf16
-  static constexpr int kQBytes = kHalves * kQHalf;
-  static constexpr int kKvHalf = kKvTile * 128;                // 64 tokens x 64 bf16
+  static constexpr int kQBytes = kHalves * kQHalf;             // one query tile
+  static constexpr int kKvHalf = kKvTile * 128;                // 128 tokens x 64 bf16
   static constexpr int kKvBytes = kHalves * kKvHalf;
-  static constexpr int kPBytes = kRows * kKvTile * 2;          // P: 128 rows x 64 tokens (one half)
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;                      // 2 stages
-  static constexpr int kV = kK + 2 * kKvBytes;                 // 2 stages
-  static constexpr int kP = kV + 2 * kKvBytes;
-  static constexpr int kTiles = kP + kPBytes;                  // 112 KB at head_dim 128
-  // + 1 KB: the barriers live in the alignment slack (below the aligned base when
-  // it is at least 256 B, else just past the tiles).  At least 80 KB, so that at
-  // most two CTAs -- 2 x 256 TMEM columns -- are resident per SM.
-  static constexpr int kSmem = (kTiles + 1024) > 80 * 1024 ? (kTiles + 1024) : 80 * 1024;
+  static constexpr int kQ = 0;                                 // 2 query tiles
+  static constexpr int kK = kQ + 2 * kQBytes;                  // kKStages stages
+  static constexpr int kV = kK + kKStages * kKvBytes;          // 2 stages
+  static constexpr int kTiles = kV + 2 * kKvBytes;             // 224 KB at head_dim 128
+  // + 1 KB: the barriers live in the alignment slack (below the aligned base when it
+  // is at least 256 B, else just past the tiles).  At least 120 KB so that one CTA
+  // (all 512 TMEM columns) is resident per SM.
+  static constexpr int kSmem = (kTiles + 1024) > 120 * 1024 ? (kTiles + 1024) : 120 * 1024;
 };
 
 // Effective (sequence length, query count) after clamping to what can be read.
@@ -92,8 +102,16 @@ __device__ __forceinline__ void pf_lengths(const PrefillParams& p, int s, int& L
   }
 }
 
+// K/V tiles a query tile needs: keys up to the position of its last valid query.
+__device__ __forceinline__ int pf_kv_tiles(int L, int q_len, int tile, int Tq) {
+  const int qi0 = tile * Tq;
+  if (qi0 >= q_len) return 0;
+  const int p_max = L - q_len + min(q_len - 1, qi0 + Tq - 1);
+  return (p_max + kKvTile) / kKvTile;
+}
+
 // ---------------------------------------------------------------------------
-// schedule: the (sequence, query tile) work list, heaviest first
+// schedule: the (sequence, query-tile pair) work list, heaviest first
 // ---------------------------------------------------------------------------
 constexpr int kSchedThreads = 1024;
 
@@ -104,11 +122,12 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   const int tid = threadIdx.x;
   const int per = (p.S + kSchedThreads - 1) / kSchedThreads;
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
+  const int pair_tokens = 2 * p.Tq;
   int local = 0;
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
     pf_lengths(p, s, L, q_len, false);
-    local += (q_len + p.Tq - 1) / p.Tq;
+    local += (q_len + pair_tokens - 1) / pair_tokens;
   }
   scan[tid] = local;
   __syncthreads();
@@ -124,11 +143,11 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
     pf_lengths(p, s, L, q_len, false);
-    const int nt = (q_len + p.Tq - 1) / p.Tq;
-    for (int t = 0; t < nt; ++t, ++pos) {
+    const int np = (q_len + pair_tokens - 1) / pair_tokens;
+    for (int t = 0; t < np; ++t, ++pos) {
       if (pos >= total) break;
-      const int p_max = L - q_len + min(q_len - 1, t * p.Tq + p.Tq - 1);
-      const int4 it = make_int4(s, t, (p_max + kKvTile) / kKvTile, 0);
+      const int work = pf_kv_tiles(L, q_len, 2 * t, p.Tq) + pf_kv_tiles(L, q_len, 2 * t + 1, p.Tq);
+      const int4 it = make_int4(s, t, work, 0);
       if (sort)
         buf[pos] = it;
       else
@@ -154,7 +173,7 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
 // main kernel
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                        const __grid_constant__ CUtensorMap tmK,
                                                                        const __grid_constant__ CUtensorMap tmV,
                                                                        const PrefillParams p) {
@@ -166,42 +185,40 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __gri
   uint8_t* sQ = smem + Sh::kQ;
   uint8_t* sK = smem + Sh::kK;
   uint8_t* sV = smem + Sh::kV;
-  uint8_t* sP = smem + Sh::kP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(slack >= 256 ? smem - 256 : smem + Sh::kTiles);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* pv_done = bars + 12;
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 15);
+  uint64_t* k_full = bars + 1;    // [kKStages]
+  uint64_t* k_empty = bars + 4;   // [kKStages]
+  uint64_t* v_full = bars + 7;    // [2 stages]
+  uint64_t* v_empty = bars + 9;   // [2 stages]
+  uint64_t* s_full = bars + 11;   // [2 groups] QK_w_j landed in S_w
+  uint64_t* p_full = bars + 13;   // [2 groups] P_w_j written over S_w (128 arrivals)
+  uint64_t* pv_done = bars + 15;  // [2 groups] PV_w_j completed
+  uint64_t* drain = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 19);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_idx = blockIdx.x / p.G, g = blockIdx.x - item_idx * p.G;
   if (item_idx >= *p.item_count) return;
   const int4 it = p.items[item_idx];
-  const int s = it.x, tile = it.y;
+  const int s = it.x, pair = it.y;
   int L, q_len;
   pf_lengths(p, s, L, q_len, threadIdx.x == 0);
-  const int qi0 = tile * p.Tq;
-  if (q_len <= 0 || qi0 >= q_len) return;
+  const int n0 = pf_kv_tiles(L, q_len, 2 * pair, p.Tq);      // K/V tiles of query tile 0
+  const int n1 = pf_kv_tiles(L, q_len, 2 * pair + 1, p.Tq);  // ... of query tile 1 (0: no second tile)
+  if (n0 <= 0) return;
+  const int n_kv = max(n0, n1);
   const int q0 = p.cu_q_lens[s];
-  const int valid_tokens = min(p.Tq, q_len - qi0);
-  const int p_min = L - q_len + qi0;             // position of the tile's first query token
-  const int p_max = p_min + valid_tokens - 1;    // ... and of its last valid one
-  const int n_kv = (p_max + kKvTile) / kKvTile;
   const int n_pages = (L + p.bs - 1) / p.bs;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], i == 11 ? 128 : 1);
+    // full barriers: one arrival per producer warp of the ring; p_full: 128 softmax threads
+    for (int i = 0; i < 18; ++i) mbar_init(&bars[i], (i == 13 || i == 14) ? 128 : ((i >= 1 && i <= 3) || (i >= 7 && i <= 8)) ? 2 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -228,70 +245,109 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __gri
   // every role calls waits with all 32 lanes: agree on the outcome before any warp-collective op
   auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp >= 8 && warp < kMmaWarp) {
+    // ------------------------------------------------------------ TMA producers
+    const int pw = warp - 8;
+    const bool is_k = pw < 2;
+    const int part = pw & 1;                   // which half of each tile's pages
     const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
-    if (lane == 0) {
+    if (pw == 0 && lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, Sh::kQBytes);
+      const int ntiles = n1 > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * Sh::kQBytes));
       const uint64_t pol = l2_policy_evict_first();
-      for (int hh = 0; hh < p.r; ++hh)
-        for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(sQ + h * Sh::kQHalf + hh * p.Tq * 128, &tmQ, q_full, h * 64, g * p.r + hh, q0 + qi0, pol);
+      for (int w = 0; w < ntiles; ++w) {
+        const int qi0 = (2 * pair + w) * p.Tq;
+        for (int hh = 0; hh < p.r; ++hh)
+          for (int h = 0; h < HALVES; ++h)
+            tma_load_3d(sQ + w * Sh::kQBytes + h * Sh::kQHalf + hh * p.Tq * 128, &tmQ, q_full, h * 64, g * p.r + hh,
+                        q0 + qi0, pol);
+      }
     }
-    const int npg = kKvTile / p.bs;  // pages per K/V tile
+    const CUtensorMap* map = is_k ? &tmK : &tmV;
+    uint8_t* ring = is_k ? sK : sV;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    const int npg = kKvTile / p.bs;            // pages per K/V tile (2, 4 or 8)
+    const int half_pg = npg >> 1;              // pages of this warp
     const uint64_t pol = l2_policy_evict_last();
+    const int depth = is_k ? kKStages : 2;
     for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      const int pg = j * npg + lane;
-      const bool live = lane < npg && pg < n_pages;
+      const int st = j % depth;
+      const int lp = part * half_pg + lane;    // page index inside the tile
+      const int pg = j * npg + lp;
+      const bool live = lane < half_pg && pg < n_pages;
       int rowc = 0;
       if (live) {
         const int b = checked_block(bt_row, pg, p.num_blocks, &g_status_prefill);
         rowc = b < 0 ? -p.bs : b * p.bs;   // a bad id reads a box entirely out of bounds: zeros
       }
       const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, live)) * p.bs * 128 * HALVES;
-      if (j >= 2 && !wait_all(&k_empty[st], ((j >> 1) - 1) & 1)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], bytes);
+      if (j >= depth && !wait_all(&empty[st], ((j / depth) - 1) & 1)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
       __syncwarp();
       if (live)
         for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(sK + st * Sh::kKvBytes + h * Sh::kKvHalf + lane * p.bs * 128, &tmK, &k_full[st], h * 64, g,
-                      rowc, pol);
-      if (j >= 2 && !wait_all(&v_empty[st], ((j >> 1) - 1) & 1)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
-      __syncwarp();
-      if (live)
-        for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(sV + st * Sh::kKvBytes + h * Sh::kKvHalf + lane * p.bs * 128, &tmV, &v_full[st], h * 64, g,
-                      rowc, pol);
+          tma_load_3d(ring + st * Sh::kKvBytes + h * Sh::kKvHalf + lp * p.bs * 128, map, &full[st], h * 64, g, rowc,
+                      pol);
     }
     if (*abort_flag) {
-      // let the loads of the last two tiles land before the CTA's memory goes away
-      for (int j = max(0, n_kv - 2); j < n_kv; ++j) {
-        mbar_wait(&k_full[j & 1], (j >> 1) & 1, &g_status_prefill);
-        mbar_wait(&v_full[j & 1], (j >> 1) & 1, &g_status_prefill);
-      }
+      // let the loads still in flight land before the CTA's memory goes away
+      for (int j = max(0, n_kv - depth); j < n_kv; ++j) mbar_wait(&full[j % depth], (j / depth) & 1, &g_status_prefill);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ UMMA issuer
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kRows, kKvTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kRows, D, false, true);
-    const uint32_t o_tmem = tmem + 2 * kKvTile;
+    const int nw[2] = {n0, n1};
     bool issued = false;
-    auto do_pv = [&](int i) -> bool {
-      const int st = i & 1;
-      if (!wait_all(p_full, i & 1)) return false;
-      if (!wait_all(&v_full[st], (i >> 1) & 1)) return false;
+    auto qk = [&](int w, int j) {  // S_w = Q_w K_j^T
+      if (lane == 0) {
+        const uint32_t qbase = smem_u32(sQ + w * Sh::kQBytes);
+        const uint32_t kbase = smem_u32(sK + (j % kKStages) * Sh::kKvBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t within = (kk & 3) * 32;
+          umma_bf16(tmem + w * kKvTile, umma_desc_sw128(qbase + (kk >> 2) * Sh::kQHalf + within, 16, 1024),
+                    umma_desc_sw128(kbase + (kk >> 2) * Sh::kKvHalf + within, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[w]);
+      }
+    };
+    auto pv = [&](int w, int j) {  // O_w += P_w V_j, P_w from the first 64 columns of S_w
+      if (lane == 0) {
+        const uint32_t vbase = smem_u32(sV + (j & 1) * Sh::kKvBytes);
+        const uint32_t o_tmem = tmem + 2 * kKvTile + w * D;
+#pragma unroll
+        for (int kk = 0; kk < kKvTile / 16; ++kk)
+          umma_bf16_tmem_a(o_tmem, tmem + w * kKvTile + kk * 8,
+                           umma_desc_sw128(vbase + kk * 2048, Sh::kKvHalf, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[w]);
+      }
+    };
+    bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+    if (ok) {
       tc_fence_after_sync();
-      const int tok0 = i * kKvTile;
+      qk(0, 0);
+      if (n1 > 0) qk(1, 0);
+      if (lane == 0) umma_commit(&k_empty[0]);  // stage of tile 0
+      issued = true;
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int vst = j & 1;
+      if (!wait_all(&v_full[vst], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int tok0 = j * kKvTile;
       if (tok0 + kKvTile > L) {
         // rows past the sequence end may hold anything (NaN included): zero them so that P = 0 stays 0
-        const int first = L - tok0;
-        uint8_t* vb = sV + st * Sh::kKvBytes;
-        for (int row = first + lane; row < kKvTile; row += 32)
+        uint8_t* vb = sV + vst * Sh::kKvBytes;
+        for (int row = (L - tok0) + lane; row < kKvTile; row += 32)
           for (int h = 0; h < HALVES; ++h) {
             uint4* d = reinterpret_cast<uint4*>(vb + h * Sh::kKvHalf + row * 128);
 #pragma unroll
@@ -300,46 +356,36 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __gri
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
-        const uint32_t pbase = smem_u32(sP);
-        const uint32_t vbase = smem_u32(sV + st * Sh::kKvBytes);
-#pragma unroll
-        for (int kk = 0; kk < kKvTile / 16; ++kk) {
-          const uint64_t a = umma_desc_sw128(pbase + kk * 32, 16, 1024);             // P: one 64-token half
-          const uint64_t b = umma_desc_sw128(vbase + kk * 2048, Sh::kKvHalf, 1024);  // V: MN-major
-          umma_bf16(o_tmem, a, b, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+      const bool more = j + 1 < n_kv;
+      bool k_ready = false;
+      for (int w = 0; w < 2; ++w) {
+        if (j < nw[w]) {
+          if (!wait_all(&p_full[w], j & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          pv(w, j);
+          // the V stage is free once the last PV of this tile has run
+          if (lane == 0 && (w == 1 || nw[1] <= j)) umma_commit(&v_empty[vst]);
         }
-        umma_commit(pv_done);
-        umma_commit(&v_empty[st]);
-      }
-      __syncwarp();
-      return true;
-    };
-    bool ok = wait_all(q_full, 0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int st = j & 1;
-      if (!wait_all(&k_full[st], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t qbase = smem_u32(sQ);
-        const uint32_t kbase = smem_u32(sK + st * Sh::kKvBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t within = (kk & 3) * 32;
-          umma_bf16(tmem + (j & 1) * kKvTile, umma_desc_sw128(qbase + (kk >> 2) * Sh::kQHalf + within, 16, 1024),
-                    umma_desc_sw128(kbase + (kk >> 2) * Sh::kKvHalf + within, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+        if (more && j + 1 < nw[w]) {
+          if (!k_ready) {  // K_{j+1} is waited for only after PV0_j is on its way
+            if (!wait_all(&k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            k_ready = true;
+          }
+          qk(w, j + 1);
         }
-        umma_commit(&s_full[j & 1]);
-        umma_commit(&k_empty[st]);
+        __syncwarp();
       }
-      issued = true;
+      if (!ok) break;
+      if (lane == 0 && more) umma_commit(&k_empty[(j + 1) % kKStages]);
       __syncwarp();
-      if (j >= 1 && !do_pv(j - 1)) ok = false;
     }
-    if (ok) ok = do_pv(n_kv - 1);
     if (!ok && issued) {
       // wait (bounded) for every UMMA this warp issued before TMEM is freed
       if (lane == 0) umma_commit(drain);
@@ -347,113 +393,123 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __gri
       mbar_wait(drain, 0, &g_status_prefill);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int row = warp * 32 + lane;
+    // ------------------------------------------------------------ softmax groups
+    const int w = warp >> 2;                    // query tile of this group
+    const int nkv = w ? n1 : n0;
+    const int row = (warp & 3) * 32 + lane;
     const int hh = row / p.Tq;
+    const int qi0 = (2 * pair + w) * p.Tq;
     const int qi = qi0 + (row - hh * p.Tq);
-    const bool row_valid = qi < q_len;
+    const bool row_valid = nkv > 0 && qi < q_len;
+    const int p_min = L - q_len + qi0;          // position of the tile's first query token
+    const int p_max = L - q_len + min(q_len - 1, qi0 + p.Tq - 1);
     const int p_row = row_valid ? (L - q_len + qi) : p_max;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t o_tmem = lane_base + 2 * kKvTile;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_tmem = lane_base + w * kKvTile;
+    const uint32_t o_tmem = lane_base + 2 * kKvTile + w * D;
     const float sl2 = p.scale_log2;
     const float sgn = sl2 < 0.f ? -1.f : 1.f;   // max of sl2 * s = |sl2| * max(sgn * s)
-    const float asl2 = fabsf(sl2);
-    uint8_t* prow = sP + row * 128;
-    const int sw = row & 7;
+    // |sl2| > 0 keeps -inf (hidden key) * |sl2| = -inf; a zero scale becomes 1e-30, which
+    // leaves every exponent equal to the max to fp32 precision (uniform weights)
+    const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) {
+    for (int j = 0; j < nkv; ++j) {
+      if (!wait_all(&s_full[w], j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      uint32_t sv[kKvTile];
-#pragma unroll
-      for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(lane_base + (j & 1) * kKvTile + c * 32, sv + c * 32);
-      tmem_ld_wait();
-      float* sc = reinterpret_cast<float*>(sv);
       const int tok0 = j * kKvTile;
-      // Visible keys of this row in this tile form a prefix: t <= p_row.  Scores stay raw
-      // (times the sign of the scale); |scale| * log2(e) is folded into the max and into
-      // one FMA per exponent.
+      // Visible keys of this row in this tile form a prefix: t <= p_row.
       const int vis = tok0 + kKvTile - 1 > p_min ? min(max(p_row - tok0 + 1, 0), kKvTile) : kKvTile;
       const bool lean = vis == kKvTile && sgn > 0.f;   // the common case: no mask, positive scale
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      if (lean) {
+      // pass 1: row max over the 128 scores, 64 columns at a time
+      float mx[8];
 #pragma unroll
-        for (int c = 0; c < kKvTile; c += 2) {
-          mx0 = fmaxf(mx0, sc[c]);
-          mx1 = fmaxf(mx1, sc[c + 1]);
-        }
-      } else {
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kKvTile; c += 2) {
-          mx0 = fmaxf(mx0, c < vis ? sc[c] * sgn : -INFINITY);
-          mx1 = fmaxf(mx1, c + 1 < vis ? sc[c + 1] * sgn : -INFINITY);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[64];
+        tmem_ld32(s_tmem + half * 64, sv);
+        tmem_ld32(s_tmem + half * 64 + 32, sv + 32);
+        tmem_ld_wait();
+        if (lean) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            mx[c & 7] = fmaxf(mx[c & 7], half * 64 + c < vis ? __uint_as_float(sv[c]) * sgn : -INFINITY);
         }
       }
-      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * asl2);
+      const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
       const bool grow = m_new > m_run + 8.0f;   // rescale only when the max grew past 2^8
       float alpha = 1.f;
       if (grow) {
         alpha = exp2_approx(m_run - m_new);
         m_run = m_new;
       }
-      if (j >= 1) {
-        // PV of the previous tile must be done: it reads P and accumulates into O
-        if (!wait_all(pv_done, (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+        // PV_w_{j-1} has completed: it was issued before QK_w_j, whose result we hold
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_tmem + c * 32, ov);
+          tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_tmem + c * 32, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(o_tmem + c * 32, ov);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(o_tmem + c * 32, ov);
         }
       }
       l_run *= alpha;
-      float lsum0 = 0.f, lsum1 = 0.f;
+      // pass 2: P = exp2(s * |sl2| - m) as bf16 pairs (even token in the low half), 64 tokens
+      // at a time, over the first 64 columns of S_w (columns already consumed)
       const float neg_m = -m_run;
+      float ls[8];
 #pragma unroll
-      for (int c8 = 0; c8 < kKvTile / 8; ++c8) {
-        float e[8];
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[64];
+        tmem_ld32(s_tmem + half * 64, sv);
+        tmem_ld32(s_tmem + half * 64 + 32, sv + 32);
+        tmem_ld_wait();
+        uint32_t pk[32];
         if (lean) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) e[i] = exp2_approx(fmaf(sc[c8 * 8 + i], asl2, neg_m));
+          for (int c = 0; c < 64; c += 2) {
+            const float e0 = exp2_approx(fmaf(__uint_as_float(sv[c]), asl2, neg_m));
+            const float e1 = exp2_approx(fmaf(__uint_as_float(sv[c + 1]), asl2, neg_m));
+            ls[c & 7] += e0;
+            ls[(c + 1) & 7] += e1;
+            pk[c >> 1] = pack_bf16x2(e0, e1);
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            e[i] = c8 * 8 + i < vis ? exp2_approx(fmaf(sc[c8 * 8 + i] * sgn, asl2, neg_m)) : 0.f;
+          for (int c = 0; c < 64; c += 2) {
+            const int t = half * 64 + c;
+            const float e0 = t < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
+            const float e1 = t + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
+            ls[c & 7] += e0;
+            ls[(c + 1) & 7] += e1;
+            pk[c >> 1] = pack_bf16x2(e0, e1);
+          }
         }
-        lsum0 += (e[0] + e[1]) + (e[2] + e[3]);
-        lsum1 += (e[4] + e[5]) + (e[6] + e[7]);
-        uint4 v;
-        v.x = pack_bf16x2(e[0], e[1]);
-        v.y = pack_bf16x2(e[2], e[3]);
-        v.z = pack_bf16x2(e[4], e[5]);
-        v.w = pack_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + (((c8 & 7) ^ sw) << 4)) = v;
+        tmem_st32(s_tmem + half * 32, pk);
       }
-      l_run += lsum0 + lsum1;
-      fence_proxy_async_smem();
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[w]);
     }
-    if (ok && wait_all(pv_done, (n_kv - 1) & 1)) {
+    if (nkv > 0 && ok && wait_all(&pv_done[w], (nkv - 1) & 1)) {
       tc_fence_after_sync();
       const float inv = 1.0f / l_run;
       const int head = g * p.r + hh;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(q0 + qi) * p.H + head) * D;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(o_tmem + c * 32, ov);
@@ -476,7 +532,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_bf16_kernel(const __gri
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -498,8 +554,9 @@ int prefill_status(uint32_t* bits, int clear) {
   return METIS_OK;
 }
 
+// (sequence, query-tile pair) items: at most ceil(T / (2 Tq)) + S
 static size_t prefill_max_items(int num_seqs, int num_tokens, int Tq) {
-  return (size_t)(num_tokens + Tq - 1) / Tq + (size_t)num_seqs;
+  return (size_t)(num_tokens + 2 * Tq - 1) / (2 * Tq) + (size_t)num_seqs;
 }
 
 template <int D>

@@ -161,8 +161,9 @@ def test_prefill_rejects(lib, kw, code):
 
 
 def test_prefill_workspace_bytes(lib):
-    # 4 heads per group -> 32-token query tiles: ceil(100 / 32) + 4 sequences = 8 tiles of 16 bytes + header
-    assert pa.metis_prefill_workspace_bytes(4, 100, 32, 8) == 256 + 8 * 16
+    # 4 heads per group -> 32-token query tiles, computed in pairs: ceil(100 / 64) + 4 sequences = 6 items
+    # of 16 bytes + a 256-byte header
+    assert pa.metis_prefill_workspace_bytes(4, 100, 32, 8) == 256 + 6 * 16
     assert pa.metis_prefill_workspace_bytes(0, 100, 32, 8) == 0
 
 
