@@ -211,16 +211,15 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
       win_next = row_coord(k + 32 + lane);
     }
     const int row = __shfl_sync(0xffffffffu, win_cur, k & 31);
-    if (lane == 0) {
-      const int st = k % STAGES;
-      uint8_t* base = smem + (warp * STAGES + st) * STAGE_BYTES;
-      uint64_t* bar = &bars[warp * STAGES + st];
-      mbar_arrive_expect_tx(bar, STAGE_BYTES);
-#pragma unroll
-      for (int h = 0; h < HALVES; ++h) tma_load_3d(base + h * kBoxBytes, &tmK, bar, h * 64, g, row, policy);
-#pragma unroll
-      for (int h = 0; h < HALVES; ++h)
-        tma_load_3d(base + (HALVES + h) * kBoxBytes, &tmV, bar, h * 64, g, row, policy);
+    const int st = k % STAGES;
+    uint8_t* base = smem + (warp * STAGES + st) * STAGE_BYTES;
+    uint64_t* bar = &bars[warp * STAGES + st];
+    if (lane == 0) mbar_arrive_expect_tx(bar, STAGE_BYTES);
+    __syncwarp();
+    // one box per lane: a single thread issues TMA instructions far slower than several
+    if (lane < 2 * HALVES) {
+      const int h = lane % HALVES;
+      tma_load_3d(base + lane * kBoxBytes, lane < HALVES ? &tmK : &tmV, bar, h * 64, g, row, policy);
     }
   };
 
