@@ -236,7 +236,8 @@ size_t metis_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads
  *
  * Supported: d_latent 512, d_rope 64; num_heads a multiple of 128, or a
  * multiple of 16 below 128; block_size 16, 32 or 64.  Tensor cores: bf16
- * operands, fp32 accumulation.
+ * operands, fp32 accumulation.  Each work item runs on a cluster of two CTAs
+ * (two SMs) that split the key dimensions and the output columns.
  */
 int metis_mla_decode(const void* q, const void* kv_cache,
                      const int32_t* block_table, const int32_t* seq_lens,

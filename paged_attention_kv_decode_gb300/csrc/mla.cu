@@ -8,20 +8,38 @@
 // the key is the full 576-wide row, the value its first 512 columns; queries
 // arrive already in latent space (the absorbed up-projection is upstream).
 //
-// Tiling.  The 128 x 512 fp32 output accumulator alone would fill all 512
-// TMEM columns, so a (sequence, partition) is computed by two CTAs, each
-// owning one 256-column half of the output: O_half (256 columns) plus a
-// double-buffered score tile S (2 x 32 columns) fit in TMEM.  Both CTAs compute
-// the same S = Q K^T (M 128 heads, N 32 tokens, K 576); the query (128 x 576
-// bf16, 144 KB) stays in shared memory, 32-token latent tiles stream through
-// a 2-stage TMA ring (128-byte swizzle), and P goes through a 64-byte-swizzled
-// tile into O_half += P V_half (N 256, K 32, V MN-major from the same tile).
+// Decomposition.  A (sequence, partition) is computed by a CLUSTER OF TWO CTAs
+// (two SMs) that split both contractions, so no product is computed twice and
+// every latent byte is read by exactly one of them:
+//   * scores: CTA r owns the key dimensions D_r = [256 r, 256 r + 256) of the
+//     latent part plus [512 + 32 r, 512 + 32 r + 32) of the rope part.  It
+//     computes the partial S_r = Q[:, D_r] K[:, D_r]^T and sends it (fp32) into
+//     its peer's shared memory (DSMEM); both add S_0 + S_1 in the same order, so
+//     both see bit-identical softmax weights;
+//   * output: CTA r owns output columns [256 r, 256 r + 256) (O_r in TMEM), whose
+//     values are exactly the latent columns it already loads for its keys.
+// Per CTA and 32-token tile that is 18 KB of latent (four 128-byte-swizzled
+// 64-column blocks plus one 64-byte-swizzled 32-column rope half block),
+// streamed through an 8-deep TMA ring.  Q_r lives in TMEM (144 columns of bf16
+// pairs, the A operand of the score UMMA), so shared memory holds only the ring
+// and double-buffered staging / receive buffers for the partial scores.  TMEM:
+// O_r 256 columns, three S buffers of 32 (P is written back over S as bf16
+// pairs), Q_r 144.
 //
-//   warp 4       TMA producer (Q once, then latent tiles)
-//   warp 5       TMEM allocation; one lane issues the UMMAs
-//   warps 0..3   softmax: one head (TMEM lane) per thread, running max in
-//                log2 units, O rescaled in TMEM only when the max grows past
-//                2^8; epilogue O / l
+//   warp 4       TMA producer (latent tiles)
+//   warp 5       TMEM allocation; one lane issues the UMMAs:
+//                  S_r = Q_r K_r^T   (M 128 heads, N 32 tokens, K 288; Q from TMEM)
+//                  O_r += P V_r      (M 128, N 256, K 32; P from TMEM)
+//   warp 6       exchange: one bulk copy per tile moves the staged partial
+//                scores into the peer's receive buffer (completing on the peer's
+//                mbarrier), and returns the credit once this CTA has read a
+//                receive buffer.  Every remote operation is on this warp, off
+//                the softmax path.
+//   warps 0..3   one head (TMEM lane) per thread: Q_r into TMEM; then per tile
+//                stage this head's partial scores of the NEXT tile (so the
+//                exchange overlaps a softmax), add the peer's partial of this
+//                tile, online softmax in log2 units (O rescaled in TMEM only
+//                when the max grows past 2^8), P back into TMEM; epilogue O_r / l
 //
 // A schedule kernel lists the (sequence, partition) work items heaviest first.
 // A sequence with one partition writes its output directly; longer ones write
@@ -31,6 +49,7 @@
 #include <algorithm>
 
 #include "../../include/metis_attn.h"
+#include "cluster.cuh"
 #include "common.cuh"
 #include "host.h"
 #include "tcgen05.cuh"
@@ -41,28 +60,32 @@ __device__ unsigned int g_status_mla = 0;
 
 constexpr int kMlaDq = 576;
 constexpr int kMlaDv = 512;
-constexpr int kMlaHalf = 256;              // output columns per CTA
-constexpr int kMlaBlocks = kMlaDq / 64;    // 64-column blocks of a latent row
-constexpr int kMlaTile = 32;               // tokens per latent tile
-constexpr int kMlaRows = 128;              // heads per CTA (the UMMA M)
-constexpr int kMlaThreads = 192;
-constexpr int kMlaTmemCols = 512;          // S0 | S1 | O_half
+constexpr int kMlaHalf = 256;       // output columns (and latent key columns) per CTA
+constexpr int kMlaTile = 32;        // tokens per latent tile
+constexpr int kMlaRows = 128;       // heads per CTA (the UMMA M)
+constexpr int kMlaThreads = 224;    // 4 softmax warps + TMA warp + MMA warp + exchange warp
+constexpr int kMlaTmemCols = 512;
 constexpr int kMlaSortMax = 2048;
+constexpr int kMlaStages = 8;       // latent tile ring depth
+constexpr int kMlaSBufs = 3;        // score buffers in TMEM
+constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
+constexpr uint32_t kTmS = 256;      // kMlaSBufs x 32 columns: S, then P (bf16 pairs) over its first 16
+constexpr uint32_t kTmQ = 352;      // 144 columns: Q_r as bf16 pairs (128 latent + 16 rope)
 
 struct MlaShape {
-  static constexpr int kQBlock = kMlaRows * 128;              // 128 heads x 64 bf16
-  static constexpr int kQBytes = kMlaBlocks * kQBlock;        // 144 KB
-  static constexpr int kKvBlock = kMlaTile * 128;             // 32 tokens x 64 bf16
-  static constexpr int kKvBytes = kMlaBlocks * kKvBlock;      // 36 KB
-  static constexpr int kQ = 0;
-  static constexpr int kKv = kQ + kQBytes;                    // 2 stages
-  static constexpr int kP = kKv + 2 * kKvBytes;               // 128 heads x 32 tokens, 64-byte rows
-  static constexpr int kPBytes = kMlaRows * 64;
-  static constexpr int kTiles = kP + kPBytes;                 // 224 KB
-  static constexpr int kSmem = kTiles + 1024;                 // barriers live in the alignment slack
+  static constexpr int kBlk = kMlaTile * 128;             // 32 tokens x 64 bf16, 128-byte swizzle
+  static constexpr int kHalf = kMlaTile * 64;             // 32 tokens x 32 bf16, 64-byte swizzle
+  static constexpr int kStage = 4 * kBlk + kHalf;         // 18 KB
+  static constexpr int kRxBuf = kMlaRows * kMlaTile * 4;  // one tile of partial scores, fp32
+  static constexpr int kKv = 0;
+  static constexpr int kRx = kKv + kMlaStages * kStage;   // two receive buffers (written by the peer)
+  static constexpr int kStg = kRx + 2 * kRxBuf;           // two staging buffers (copied to the peer)
+  static constexpr int kBars = kStg + 2 * kRxBuf;         // 208 KB of tiles, then the barriers
+  static constexpr int kSmem = kBars + 512 + 1024;        // + alignment slack
 };
 
 struct MlaParams {
+  const uint4* q;   // [S, H, 576] bf16, read as 16-byte chunks
   const int32_t* block_table;
   const int32_t* seq_lens;
   void* out;
@@ -131,39 +154,46 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, i
   if (tid == 0) *count = total;
 }
 
-__global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                                     const __grid_constant__ CUtensorMap tmKV,
-                                                                     const MlaParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKVh,
+                      const MlaParams p) {
   using Sh = MlaShape;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t slack = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + slack;
-  uint8_t* sQ = smem + Sh::kQ;
   uint8_t* sKV = smem + Sh::kKv;
-  uint8_t* sP = smem + Sh::kP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(slack >= 256 ? smem - 256 : smem + Sh::kTiles);
-  uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* pv_done = bars + 8;
-  uint64_t* drain = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 11);
+  float* sRx = reinterpret_cast<float*>(smem + Sh::kRx);
+  float* sStg = reinterpret_cast<float*>(smem + Sh::kStg);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBars);
+  uint64_t* kv_full = bars + 0;    // [kMlaStages]
+  uint64_t* kv_empty = bars + 8;   // [kMlaStages]
+  uint64_t* s_full = bars + 16;    // [kMlaSBufs] partial S_j landed
+  uint64_t* p_full = bars + 19;    // [kMlaSBufs] P_j written over S (128 arrivals)
+  // [kMlaSBufs] PV_j completed, on barrier j % 3: at most PV_{j-2} and PV_{j-1} are
+  // outstanding when tile j is processed, so a parity wait there is unambiguous
+  uint64_t* pv_done = bars + 22;
+  uint64_t* staged = bars + 25;    // [2] partial scores of a tile are in sStg (128 arrivals)
+  uint64_t* rx_read = bars + 27;   // [2] this CTA has read a receive buffer (128 arrivals)
+  uint64_t* rx_full = bars + 29;   // [2] the peer's partial scores are in sRx (armed with expect_tx)
+  uint64_t* tx_ok = bars + 31;     // [2] the peer has read the tile we copied into it (1 remote arrival)
+  uint64_t* q_full = bars + 33;    // Q_r is in TMEM (128 arrivals)
+  uint64_t* drain = bars + 34;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 35);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 36);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = blockIdx.x & 1;
+  const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
+  const uint32_t peer = rank ^ 1u;
   const int rest = blockIdx.x >> 1;
   const int ht = rest % p.head_tiles;
   const int item_idx = rest / p.head_tiles;
-  if (item_idx >= *p.item_count) return;
+  if (item_idx >= *p.item_count) return;  // both CTAs of the cluster take the same branch
   const int4 it = p.items[item_idx];
   const int s = it.x, part = it.y;
   const int L_raw = p.seq_lens[s];
   int L = L_raw;
   if (L > p.cap) {
-    if (threadIdx.x == 0 && half == 0 && ht == 0 && part == 0) atomicOr(&g_status_mla, METIS_STATUS_SEQ_TOO_LONG);
+    if (threadIdx.x == 0 && rank == 0 && ht == 0 && part == 0) atomicOr(&g_status_mla, METIS_STATUS_SEQ_TOO_LONG);
     L = p.cap;
   }
   if (L < 0) L = 0;
@@ -178,10 +208,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
       if (head >= p.H) continue;
       const size_t sh = (size_t)s * p.H + head;
       if (direct) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + half * kMlaHalf;
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf;
         for (int c = 0; c < kMlaHalf; ++c) o[c] = __float2bfloat16(0.f);
-        if (half == 0 && p.lse_out) p.lse_out[sh] = -INFINITY;
-      } else if (half == 0) {
+        if (rank == 0 && p.lse_out) p.lse_out[sh] = -INFINITY;
+      } else if (rank == 0) {
         p.part_lse[sh * p.max_parts + part] = -INFINITY;
       }
     }
@@ -191,27 +221,32 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
   const int n_pages = (L + p.bs - 1) / p.bs;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 10; ++i) mbar_init(&bars[i], i == 7 ? 128 : 1);
+    for (int i = 0; i < 35; ++i) mbar_init(&bars[i], (i >= 19 && i <= 21) || (i >= 25 && i <= 28) || i == 33 ? 128 : 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // arm the receive buffers for tiles 0 and 1
+    mbar_arrive_expect_tx(&rx_full[0], Sh::kRxBuf);
+    mbar_arrive_expect_tx(&rx_full[1], Sh::kRxBuf);
   }
   if (warp == 5) {
     tmem_alloc(tmem_slot, kMlaTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // A wait that also gives up when another role has aborted.  Cluster-scope
+  // acquire so that the peer's DSMEM writes released by its arrivals are visible.
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t tstart = global_timer_ns();
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t ts = global_timer_ns();
     for (uint32_t i = 1; i < kMaxPolls; ++i) {
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_cluster(bar, parity)) return true;
       if ((i & 255u) == 0) {
         if (*abort_flag) return false;
-        if (global_timer_ns() - tstart > kMaxWaitNs) break;
+        if (global_timer_ns() - ts > kMaxWaitNs) break;
       }
     }
     atomicOr(&g_status_mla, METIS_STATUS_WAIT_TIMEOUT);
@@ -222,55 +257,92 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
+    // Per tile and page piece: lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3,
+    // lane 5 pi + 4 the rope half block 512 + 32 r .. + 31.
     const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmKV);
-      mbar_arrive_expect_tx(q_full, (uint32_t)(kMlaBlocks * p.hrows * 128));
-      const uint64_t pol = l2_policy_evict_first();
-      for (int b = 0; b < kMlaBlocks; ++b) tma_load_3d(sQ + b * Sh::kQBlock, &tmQ, q_full, b * 64, h0, s, pol);
+      tma_prefetch_desc(&tmKVh);
     }
-    const int R = min(p.bs, kMlaTile);    // rows per box
-    const int boxes = kMlaTile / R;       // boxes per tile
+    const int R = min(p.bs, kMlaTile);  // rows per box
+    const int pieces = kMlaTile / R;
+    const int pi = lane / 5, lb = lane - pi * 5;
     const uint64_t pol = l2_policy_evict_first();
+    int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      const int tok = t0 + j * kMlaTile + lane * R;
+      const int st = j % kMlaStages;
+      const int tok = t0 + j * kMlaTile + pi * R;
       const int pg = tok / p.bs;
-      const bool live = lane < boxes && pg < n_pages;
+      const bool live = pi < pieces && pg < n_pages;
       int rowc = 0;
       if (live) {
         const int b = checked_block(bt_row, pg, p.num_blocks, &g_status_mla);
         rowc = b < 0 ? -R : b * p.bs + (tok - pg * p.bs);
       }
-      const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, live)) * R * 128 * kMlaBlocks;
-      if (j >= 2 && !wait_all(&kv_empty[st], ((j >> 1) - 1) & 1)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], bytes);
+      const uint32_t n_live = (uint32_t)__popc(__ballot_sync(0xffffffffu, live && lb == 0));
+      if (j >= kMlaStages && !wait_all(&kv_empty[st], ((j / kMlaStages) - 1) & 1)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], n_live * (uint32_t)(R * (4 * 128 + 64)));
       __syncwarp();
-      if (live)
-        for (int b = 0; b < kMlaBlocks; ++b)
-          tma_load_3d(sKV + st * Sh::kKvBytes + b * Sh::kKvBlock + lane * R * 128, &tmKV, &kv_full[st], b * 64, 0,
-                      rowc, pol);
+      if (live) {
+        uint8_t* dst = sKV + st * Sh::kStage;
+        if (lb < 4)
+          tma_load_3d(dst + lb * Sh::kBlk + pi * R * 128, &tmKV, &kv_full[st], (4 * (int)rank + lb) * 64, 0, rowc,
+                      pol);
+        else
+          tma_load_3d(dst + 4 * Sh::kBlk + pi * R * 64, &tmKVh, &kv_full[st], kMlaDv + 32 * (int)rank, 0, rowc, pol);
+      }
+      ++issued;
     }
     if (*abort_flag)
-      for (int j = max(0, n_tiles - 2); j < n_tiles; ++j) mbar_wait(&kv_full[j & 1], (j >> 1) & 1, &g_status_mla);
+      for (int j = max(0, issued - kMlaStages); j < issued; ++j)
+        mbar_wait(&kv_full[j % kMlaStages], (j / kMlaStages) & 1, &g_status_mla);
   } else if (warp == 5) {
     // ------------------------------------------------------------ UMMA issuer
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kMlaRows, kMlaTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kMlaRows, kMlaHalf, false, true);
-    const uint32_t o_tmem = tmem + 2 * kMlaTile;
     bool issued = false;
-    auto do_pv = [&](int i) -> bool {
-      const int st = i & 1;
-      if (!wait_all(p_full, i & 1)) return false;
+    auto qk = [&](int j) {  // partial S_j = Q_r K_r^T over this CTA's 288 key dimensions
+      if (lane == 0) {
+        const uint32_t kb = smem_u32(sKV + (j % kMlaStages) * Sh::kStage);
+        const uint32_t d_tmem = tmem + kTmS + (j % kMlaSBufs) * kMlaTile;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          umma_bf16_tmem_a(d_tmem, tmem + kTmQ + kk * 8,
+                           umma_desc_sw128(kb + (kk >> 2) * Sh::kBlk + (kk & 3) * 32, 16, 1024), kIdQK,
+                           kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          umma_bf16_tmem_a(d_tmem, tmem + kTmQ + 128 + kk * 8, umma_desc_sw64(kb + 4 * Sh::kBlk + kk * 32, 512), kIdQK,
+                           1u);
+        umma_commit(&s_full[j % kMlaSBufs]);
+      }
+    };
+    bool ok = wait_all(q_full, 0);
+    if (ok) tc_fence_after_sync();
+    for (int j = 0; ok && j < kMlaSBufs && j < n_tiles; ++j) {
+      if (!wait_all(&kv_full[j % kMlaStages], (j / kMlaStages) & 1)) {
+        ok = false;
+        break;
+      }
       tc_fence_after_sync();
-      const int tok0 = t0 + i * kMlaTile;
-      uint8_t* vb = sKV + st * Sh::kKvBytes + half * 4 * Sh::kKvBlock;
+      qk(j);
+      issued = true;
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int st = j % kMlaStages, sb = j % kMlaSBufs;
+      if (!wait_all(&p_full[sb], (j / kMlaSBufs) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int tok0 = t0 + j * kMlaTile;
       if (tok0 + kMlaTile > t1) {
-        // rows past the partition end (NaN tails, pages not loaded): zero this half's value columns
+        // rows past the partition end (NaN tails, pieces not loaded): zero the value columns
+        uint8_t* vb = sKV + st * Sh::kStage;
         for (int row = (t1 - tok0) + lane; row < kMlaTile; row += 32)
           for (int b = 0; b < 4; ++b) {
-            uint4* d = reinterpret_cast<uint4*>(vb + b * Sh::kKvBlock + row * 128);
+            uint4* d = reinterpret_cast<uint4*>(vb + b * Sh::kBlk + row * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
           }
@@ -278,47 +350,55 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         __syncwarp();
       }
       if (lane == 0) {
-        const uint32_t pbase = smem_u32(sP);
-        const uint32_t vbase = smem_u32(vb);
+        const uint32_t vbase = smem_u32(sKV + st * Sh::kStage);
 #pragma unroll
         for (int kk = 0; kk < kMlaTile / 16; ++kk)
-          umma_bf16(o_tmem, umma_desc_sw64(pbase + kk * 32, 512), umma_desc_sw128(vbase + kk * 2048, Sh::kKvBlock, 1024),
-                    kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(pv_done);
+          umma_bf16_tmem_a(tmem + kTmO, tmem + kTmS + sb * kMlaTile + kk * 8,
+                           umma_desc_sw128(vbase + kk * 2048, Sh::kBlk, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[sb]);
         umma_commit(&kv_empty[st]);
       }
       __syncwarp();
-      return true;
-    };
-    bool ok = wait_all(q_full, 0);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int st = j & 1;
-      if (!wait_all(&kv_full[st], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t qbase = smem_u32(sQ);
-        const uint32_t kbase = smem_u32(sKV + st * Sh::kKvBytes);
-#pragma unroll 4
-        for (int kk = 0; kk < kMlaDq / 16; ++kk) {
-          const uint32_t within = (kk & 3) * 32;
-          umma_bf16(tmem + (j & 1) * kMlaTile,
-                    umma_desc_sw128(qbase + (kk >> 2) * Sh::kQBlock + within, 16, 1024),
-                    umma_desc_sw128(kbase + (kk >> 2) * Sh::kKvBlock + within, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+      const int jn = j + kMlaSBufs;  // QK_jn overwrites S[sb] after PV_j (in issue order)
+      if (jn < n_tiles) {
+        if (!wait_all(&kv_full[jn % kMlaStages], (jn / kMlaStages) & 1)) {
+          ok = false;
+          break;
         }
-        umma_commit(&s_full[j & 1]);
+        tc_fence_after_sync();
+        qk(jn);
+        __syncwarp();
       }
-      issued = true;
-      __syncwarp();
-      if (j >= 1 && !do_pv(j - 1)) ok = false;
     }
-    if (ok) ok = do_pv(n_tiles - 1);
     if (!ok && issued) {
       if (lane == 0) umma_commit(drain);
       __syncwarp();
       mbar_wait(drain, 0, &g_status_mla);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ exchange warp
+    const uint32_t peer_rx = dsmem_map(smem_u32(sRx), peer);
+    const uint32_t peer_rx_full = dsmem_map(smem_u32(rx_full), peer);
+    const uint32_t peer_tx_ok = dsmem_map(smem_u32(tx_ok), peer);
+    for (int t = 0; t <= n_tiles; ++t) {
+      if (t < n_tiles) {  // staged tile t -> the peer's receive buffer t & 1
+        const int b = t & 1;
+        if (!wait_all(&staged[b], (t >> 1) & 1)) break;
+        if (lane == 0)
+          bulk_copy_to_peer(peer_rx + b * Sh::kRxBuf, smem_u32(sStg) + b * Sh::kRxBuf, Sh::kRxBuf, peer_rx_full + b * 8);
+        __syncwarp();
+      }
+      const int u = t - 1;  // credit: this CTA has read tile u, so the peer may send tile u + 2
+      if (u >= 0 && u + 2 < n_tiles) {
+        const int b = u & 1;
+        if (!wait_all(&rx_read[b], (u >> 1) & 1)) break;
+        // Relaxed: the only thing the credit must order is the softmax threads' reads
+        // of the receive buffer, and those have returned before their rx_read arrival
+        // (release), so the peer's next copy cannot overtake them.  A cluster-scope
+        // release here would also wait for the bulk copy issued just before.
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_tx_ok + b * 8);
+        __syncwarp();
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -326,91 +406,156 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     const int head = h0 + row;
     const bool row_valid = row < p.hrows && head < p.H;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t o_tmem = lane_base + 2 * kMlaTile;
+    {
+      // Q_r of this head into TMEM columns kTmQ.. as bf16 pairs (the raw row words):
+      // latent dims 256 r .. 256 r + 255, then rope dims 512 + 32 r .. + 31.
+      const uint4* src = p.q + ((size_t)s * p.H + (row_valid ? head : 0)) * (kMlaDq / 8);
+      uint32_t qa[64];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 v = row_valid ? __ldg(src + 32 * rank + i) : make_uint4(0u, 0u, 0u, 0u);
+        qa[4 * i] = v.x, qa[4 * i + 1] = v.y, qa[4 * i + 2] = v.z, qa[4 * i + 3] = v.w;
+      }
+      uint32_t qb[80];
+#pragma unroll
+      for (int i = 0; i < 20; ++i) {
+        const int idx = i < 16 ? 32 * rank + 16 + i : kMlaDv / 8 + 4 * rank + (i - 16);
+        const uint4 v = row_valid ? __ldg(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+        qb[4 * i] = v.x, qb[4 * i + 1] = v.y, qb[4 * i + 2] = v.z, qb[4 * i + 3] = v.w;
+      }
+      tmem_st32(lane_base + kTmQ, qa);
+      tmem_st32(lane_base + kTmQ + 32, qa + 32);
+      tmem_st32(lane_base + kTmQ + 64, qb);
+      tmem_st32(lane_base + kTmQ + 96, qb + 32);
+      tmem_st16(lane_base + kTmQ + 128, qb + 64);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(q_full);
+    }
     const float sl2 = p.scale_log2;
     const float sgn = sl2 < 0.f ? -1.f : 1.f;
-    const float asl2 = fabsf(sl2);
-    uint8_t* prow = sP + row * 64;
-    const int sw = (row >> 1) & 3;
+    const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
+    // staging / receive rows of this head: 8 chunks of 4 floats, chunk c stored at
+    // c ^ (row & 7) so that the 8 rows a quarter-warp touches hit distinct banks
+    const int rsw = row & 7;
+    float* my_stg = sStg + row * kMlaTile;
+    const float* my_rx = sRx + row * kMlaTile;
+    auto load_s = [&](int t, uint32_t* v) -> bool {  // this CTA's partial scores of tile t
+      if (!wait_all(&s_full[t % kMlaSBufs], (t / kMlaSBufs) & 1)) return false;
+      tc_fence_after_sync();
+      tmem_ld32(lane_base + kTmS + (t % kMlaSBufs) * kMlaTile, v);
+      tmem_ld_wait();
+      return true;
+    };
+    auto stage = [&](int t, const uint32_t* v) -> bool {  // into staging buffer t & 1 for the exchange warp
+      const int b = t & 1;
+      // the copy of tile t - 2 out of this buffer has landed (the peer has even read it)
+      if (t >= 2 && !wait_all(&tx_ok[b], ((t >> 1) - 1) & 1)) return false;
+      float* dst = my_stg + b * (Sh::kRxBuf / 4);
+#pragma unroll
+      for (int c = 0; c < kMlaTile / 4; ++c)
+        *reinterpret_cast<uint4*>(dst + ((c ^ rsw) << 2)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();  // the bulk copy reads through the async proxy
+      mbar_arrive(&staged[b]);
+      return true;
+    };
+    uint32_t cur[kMlaTile], nxt[kMlaTile];
+    int armed0 = 0, armed1 = n_tiles > 1 ? 1 : -1;  // newest tile each receive buffer is armed for (thread 0)
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) {
+    bool ok = load_s(0, cur) && stage(0, cur);
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (j + 1 < n_tiles && !(load_s(j + 1, nxt) && stage(j + 1, nxt))) {
         ok = false;
         break;
       }
-      tc_fence_after_sync();
-      uint32_t sv[kMlaTile];
-      tmem_ld32(lane_base + (j & 1) * kMlaTile, sv);
-      tmem_ld_wait();
-      const float* sc = reinterpret_cast<const float*>(sv);
-      const int vis = min(kMlaTile, t1 - (t0 + j * kMlaTile));
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kMlaTile; c += 2) {
-        mx0 = fmaxf(mx0, c < vis ? sc[c] * sgn : -INFINITY);
-        mx1 = fmaxf(mx1, c + 1 < vis ? sc[c + 1] * sgn : -INFINITY);
+      const int b = j & 1, sb = j % kMlaSBufs;
+      if (!wait_all(&rx_full[b], (j >> 1) & 1)) {
+        ok = false;
+        break;
       }
-      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * asl2);
+      float sc[kMlaTile];
+      const float* rx = my_rx + b * (Sh::kRxBuf / 4);
+#pragma unroll
+      for (int c = 0; c < kMlaTile / 4; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(rx + ((c ^ rsw) << 2));
+        sc[4 * c] = __uint_as_float(cur[4 * c]) + v.x;
+        sc[4 * c + 1] = __uint_as_float(cur[4 * c + 1]) + v.y;
+        sc[4 * c + 2] = __uint_as_float(cur[4 * c + 2]) + v.z;
+        sc[4 * c + 3] = __uint_as_float(cur[4 * c + 3]) + v.w;
+      }
+      mbar_arrive(&rx_read[b]);
+      // re-arm buffer b for tile j + 2: its data cannot arrive before every thread here
+      // has read tile j (the peer waits for the credit that rx_read leads to)
+      if (threadIdx.x == 0 && j + 2 < n_tiles) {
+        mbar_arrive_expect_tx(&rx_full[b], Sh::kRxBuf);
+        if (b) armed1 = j + 2;
+        else armed0 = j + 2;
+      }
+      const int vis = min(kMlaTile, t1 - (t0 + j * kMlaTile));
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMlaTile; ++c) mx[c & 7] = fmaxf(mx[c & 7], c < vis ? sc[c] * sgn : -INFINITY);
+      const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
       const bool grow = m_new > m_run + 8.0f;
       float alpha = 1.f;
       if (grow) {
         alpha = exp2_approx(m_run - m_new);
         m_run = m_new;
       }
-      if (j >= 1) {
-        if (!wait_all(pv_done, (j - 1) & 1)) {
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+        // O_r holds PV_{j-1} only once that UMMA completed (PV_j is not issued yet)
+        if (!wait_all(&pv_done[(j - 1) % kMlaSBufs], ((j - 1) / kMlaSBufs) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int c = 0; c < kMlaHalf / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_tmem + c * 32, ov);
-            tmem_ld_wait();
+        for (int c = 0; c < kMlaHalf / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + kTmO + c * 32, ov);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(o_tmem + c * 32, ov);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(lane_base + kTmO + c * 32, ov);
         }
       }
       l_run *= alpha;
-      float lsum = 0.f;
       const float neg_m = -m_run;
+      float ls[8];
 #pragma unroll
-      for (int c8 = 0; c8 < kMlaTile / 8; ++c8) {
-        float e[8];
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+      uint32_t pk[kMlaTile / 2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          e[i] = c8 * 8 + i < vis ? exp2_approx(fmaf(sc[c8 * 8 + i] * sgn, asl2, neg_m)) : 0.f;
-        lsum += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-        uint4 v;
-        v.x = pack_bf16x2(e[0], e[1]);
-        v.y = pack_bf16x2(e[2], e[3]);
-        v.z = pack_bf16x2(e[4], e[5]);
-        v.w = pack_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ sw) << 4)) = v;
+      for (int c = 0; c < kMlaTile; c += 2) {
+        const float e0 = c < vis ? exp2_approx(fmaf(sc[c] * sgn, asl2, neg_m)) : 0.f;
+        const float e1 = c + 1 < vis ? exp2_approx(fmaf(sc[c + 1] * sgn, asl2, neg_m)) : 0.f;
+        ls[c & 7] += e0;
+        ls[(c + 1) & 7] += e1;
+        pk[c >> 1] = pack_bf16x2(e0, e1);
       }
-      l_run += lsum;
-      fence_proxy_async_smem();
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      tmem_st16(lane_base + kTmS + sb * kMlaTile, pk);
+      tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[sb]);
+#pragma unroll
+      for (int c = 0; c < kMlaTile; ++c) cur[c] = nxt[c];
     }
-    if (ok && wait_all(pv_done, (n_tiles - 1) & 1)) {
+    if (ok && wait_all(&pv_done[(n_tiles - 1) % kMlaSBufs], ((n_tiles - 1) / kMlaSBufs) & 1)) {
       tc_fence_after_sync();
       const float inv = 1.0f / l_run;
       const size_t sh = (size_t)s * p.H + head;
 #pragma unroll 1
       for (int c = 0; c < kMlaHalf / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(o_tmem + c * 32, ov);
+        tmem_ld32(lane_base + kTmO + c * 32, ov);
         tmem_ld_wait();
         if (!row_valid) continue;
         if (direct) {
-          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + half * kMlaHalf + c * 32;
+          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf + c * 32;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 v;
@@ -421,7 +566,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             *reinterpret_cast<uint4*>(o + i) = v;
           }
         } else {
-          float* o = p.part_out + (sh * p.max_parts + part) * kMlaDv + half * kMlaHalf + c * 32;
+          float* o = p.part_out + (sh * p.max_parts + part) * kMlaDv + rank * kMlaHalf + c * 32;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(o + i) =
@@ -429,7 +574,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                             __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
         }
       }
-      if (row_valid && half == 0) {
+      if (row_valid && rank == 0) {
         const float lse = (m_run + log2f(l_run)) * kLn2;
         if (direct) {
           if (p.lse_out) p.lse_out[sh] = lse;
@@ -437,6 +582,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
           p.part_lse[sh * p.max_parts + part] = lse;
         }
       }
+    }
+    // after an abort, let the peer's copies already on their way land before this CTA exits
+    if (threadIdx.x == 0 && *abort_flag) {
+      if (armed0 >= 0) mbar_wait(&rx_full[0], (armed0 >> 1) & 1, &g_status_mla);
+      if (armed1 >= 0) mbar_wait(&rx_full[1], (armed1 >> 1) & 1, &g_status_mla);
     }
   }
 
@@ -446,6 +596,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     tc_fence_after_sync();
     tmem_dealloc(tmem, kMlaTmemCols);
   }
+  cluster_sync_all();  // no DSMEM access may target a CTA that has exited
 }
 
 // ---------------------------------------------------------------------------
@@ -525,6 +676,7 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   if (lay.max_items * head_tiles * 2 > 0x7fffffffull) return fail(METIS_E_SHAPE, "too many work items");
 
   MlaParams p{};
+  p.q = reinterpret_cast<const uint4*>(q);
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.out = out;
@@ -549,17 +701,16 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   p.scale_log2 = scale * kLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  CUtensorMap tmQ, tmKV;
-  const uint64_t qdims[3] = {(uint64_t)kMlaDq, (uint64_t)num_heads, (uint64_t)num_seqs};
-  const uint64_t qstr[2] = {(uint64_t)kMlaDq * 2, (uint64_t)num_heads * kMlaDq * 2};
-  const uint32_t qbox[3] = {64, (uint32_t)p.hrows, 1};
-  int rc = encode_tiled(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, qdims, qstr, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc) return rc;
+  CUtensorMap tmKV, tmKVh;
   const uint64_t kdims[3] = {(uint64_t)kMlaDq, 1, (uint64_t)num_blocks * block_size};
   const uint64_t kstr[2] = {(uint64_t)kMlaDq * 2, (uint64_t)kMlaDq * 2};
   const uint32_t kbox[3] = {64, 1, (uint32_t)std::min(block_size, kMlaTile)};
-  rc = encode_tiled(&tmKV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, kbox,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = encode_tiled(&tmKV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, kbox,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  const uint32_t khbox[3] = {32, 1, (uint32_t)std::min(block_size, kMlaTile)};
+  rc = encode_tiled(&tmKVh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, khbox,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
 
   mla_schedule_kernel<<<1, 1024, 0, st>>>(p, items, count, (int)lay.max_items);
@@ -568,7 +719,7 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   static int done = 0;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), MlaShape::kSmem, &done);
   if (rc) return rc;
-  mla_decode_kernel<<<(unsigned)(lay.max_items * head_tiles * 2), kMlaThreads, MlaShape::kSmem, st>>>(tmQ, tmKV, p);
+  mla_decode_kernel<<<(unsigned)(lay.max_items * head_tiles * 2), kMlaThreads, MlaShape::kSmem, st>>>(tmKV, tmKVh, p);
   rc = check_launch("mla_decode_kernel launch");
   if (rc) return rc;
   if (partition_size > 0 && lay.max_parts > 1)
