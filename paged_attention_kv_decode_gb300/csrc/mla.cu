@@ -18,27 +18,33 @@
 //     both see bit-identical softmax weights;
 //   * output: CTA r owns output columns [256 r, 256 r + 256) (O_r in TMEM), whose
 //     values are exactly the latent columns it already loads for its keys.
-// Per CTA and 32-token tile that is 18 KB of latent (four 128-byte-swizzled
-// 64-column blocks plus one 64-byte-swizzled 32-column rope half block),
-// streamed through an 8-deep TMA ring.  Q_r lives in TMEM (144 columns of bf16
-// pairs, the A operand of the score UMMA), so shared memory holds only the ring
-// and double-buffered staging / receive buffers for the partial scores.  TMEM:
-// O_r 256 columns, three S buffers of 32 (P is written back over S as bf16
-// pairs), Q_r 144.
 //
-//   warp 4       TMA producer (latent tiles)
+// Granularity.  A UMMA costs at least ~46 cycles whatever its N, so N = 32
+// wastes two thirds of the tensor pipe: the scores are computed for 64-token
+// tiles (N = 64).  Softmax, the score exchange and P V run on 32-token units,
+// two per tile.  Per CTA and unit that is 18 KB of latent (four
+// 128-byte-swizzled 64-column blocks plus one 64-byte-swizzled 32-column rope
+// half block), streamed through an 8-unit TMA ring laid out block-major, so
+// that the two units of a tile are one contiguous 64-row operand per block.
+//
+// TMEM (512 columns): O_r 256 | S 2 x 64 (P of a unit is written back over the
+// scores as bf16 pairs) | the latent part of Q_r, 128 columns of bf16 pairs (the
+// A operand of the score UMMA).  The rope part of Q_r (32 dimensions) sits in
+// shared memory.
+//
+//   warp 4       TMA producer (latent units)
 //   warp 5       TMEM allocation; one lane issues the UMMAs:
-//                  S_r = Q_r K_r^T   (M 128 heads, N 32 tokens, K 288; Q from TMEM)
-//                  O_r += P V_r      (M 128, N 256, K 32; P from TMEM)
-//   warp 6       exchange: one bulk copy per tile moves the staged partial
+//                  S_r = Q_r K_r^T   (M 128 heads, N 64 tokens, K 288)
+//                  O_r += P V_r      (M 128, N 256, K 32 per unit; P from TMEM)
+//   warp 6       exchange: one bulk copy per unit moves the staged partial
 //                scores into the peer's receive buffer (completing on the peer's
 //                mbarrier), and returns the credit once this CTA has read a
 //                receive buffer.  Every remote operation is on this warp, off
 //                the softmax path.
-//   warps 0..3   one head (TMEM lane) per thread: Q_r into TMEM; then per tile
-//                stage this head's partial scores of the NEXT tile (so the
-//                exchange overlaps a softmax), add the peer's partial of this
-//                tile, online softmax in log2 units (O rescaled in TMEM only
+//   warps 0..3   one head (TMEM lane) per thread: Q_r into TMEM / shared memory;
+//                then per unit stage this head's partial scores of the NEXT unit
+//                (so the exchange overlaps a softmax), add the peer's partial of
+//                this unit, online softmax in log2 units (O rescaled in TMEM only
 //                when the max grows past 2^8), P back into TMEM; epilogue O_r / l
 //
 // A schedule kernel lists the (sequence, partition) work items heaviest first.
@@ -61,26 +67,27 @@ __device__ unsigned int g_status_mla = 0;
 constexpr int kMlaDq = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaHalf = 256;       // output columns (and latent key columns) per CTA
-constexpr int kMlaTile = 32;        // tokens per latent tile
+constexpr int kMlaUnit = 32;        // tokens per softmax / exchange / P V unit and per ring stage
+constexpr int kMlaTile = 64;        // tokens per score UMMA (two units)
 constexpr int kMlaRows = 128;       // heads per CTA (the UMMA M)
 constexpr int kMlaThreads = 224;    // 4 softmax warps + TMA warp + MMA warp + exchange warp
 constexpr int kMlaTmemCols = 512;
 constexpr int kMlaSortMax = 2048;
-constexpr int kMlaStages = 8;       // latent tile ring depth
-constexpr int kMlaSBufs = 3;        // score buffers in TMEM
+constexpr int kMlaStages = 8;       // ring stages of one unit (even: a tile is two adjacent stages)
 constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
-constexpr uint32_t kTmS = 256;      // kMlaSBufs x 32 columns: S, then P (bf16 pairs) over its first 16
-constexpr uint32_t kTmQ = 352;      // 144 columns: Q_r as bf16 pairs (128 latent + 16 rope)
+constexpr uint32_t kTmS = 256;      // 2 x 64 columns: S, then P (bf16 pairs, 16 columns per unit)
+constexpr uint32_t kTmQ = 384;      // 128 columns: latent part of Q_r as bf16 pairs
 
 struct MlaShape {
-  static constexpr int kBlk = kMlaTile * 128;             // 32 tokens x 64 bf16, 128-byte swizzle
-  static constexpr int kHalf = kMlaTile * 64;             // 32 tokens x 32 bf16, 64-byte swizzle
-  static constexpr int kStage = 4 * kBlk + kHalf;         // 18 KB
-  static constexpr int kRxBuf = kMlaRows * kMlaTile * 4;  // one tile of partial scores, fp32
-  static constexpr int kKv = 0;
-  static constexpr int kRx = kKv + kMlaStages * kStage;   // two receive buffers (written by the peer)
+  static constexpr int kBlk = kMlaUnit * 128;             // one unit of one 64-column block (128-byte swizzle)
+  static constexpr int kRopeU = kMlaUnit * 64;            // one unit of the rope half block (64-byte swizzle)
+  static constexpr int kRxBuf = kMlaRows * kMlaUnit * 4;  // one unit of partial scores, fp32
+  static constexpr int kKv = 0;                           // block b of stage s at kKv + (b * kMlaStages + s) * kBlk
+  static constexpr int kRope = kKv + 4 * kMlaStages * kBlk;  // stage s at kRope + s * kRopeU
+  static constexpr int kQr = kRope + kMlaStages * kRopeU;    // rope part of Q_r: 128 rows x 64 B, 64-byte swizzle
+  static constexpr int kRx = kQr + kMlaRows * 64;         // two receive buffers (written by the peer)
   static constexpr int kStg = kRx + 2 * kRxBuf;           // two staging buffers (copied to the peer)
-  static constexpr int kBars = kStg + 2 * kRxBuf;         // 208 KB of tiles, then the barriers
+  static constexpr int kBars = kStg + 2 * kRxBuf;         // 216 KB, then the barriers
   static constexpr int kSmem = kBars + 512 + 1024;        // + alignment slack
 };
 
@@ -162,24 +169,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const uint32_t slack = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + slack;
   uint8_t* sKV = smem + Sh::kKv;
+  uint8_t* sRope = smem + Sh::kRope;
+  uint8_t* sQr = smem + Sh::kQr;
   float* sRx = reinterpret_cast<float*>(smem + Sh::kRx);
   float* sStg = reinterpret_cast<float*>(smem + Sh::kStg);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBars);
   uint64_t* kv_full = bars + 0;    // [kMlaStages]
   uint64_t* kv_empty = bars + 8;   // [kMlaStages]
-  uint64_t* s_full = bars + 16;    // [kMlaSBufs] partial S_j landed
-  uint64_t* p_full = bars + 19;    // [kMlaSBufs] P_j written over S (128 arrivals)
-  // [kMlaSBufs] PV_j completed, on barrier j % 3: at most PV_{j-2} and PV_{j-1} are
-  // outstanding when tile j is processed, so a parity wait there is unambiguous
+  uint64_t* s_full = bars + 16;    // [2] scores of tile j landed in S[j & 1]
+  // [4] P of unit u written (128 arrivals) / P V of unit u completed, on barrier u % 4:
+  // at most three P V units are outstanding while unit u is processed, and the
+  // softmax never runs four units ahead of the UMMA issuer, so parity waits on
+  // these are unambiguous
+  uint64_t* p_full = bars + 18;
   uint64_t* pv_done = bars + 22;
-  uint64_t* staged = bars + 25;    // [2] partial scores of a tile are in sStg (128 arrivals)
-  uint64_t* rx_read = bars + 27;   // [2] this CTA has read a receive buffer (128 arrivals)
-  uint64_t* rx_full = bars + 29;   // [2] the peer's partial scores are in sRx (armed with expect_tx)
-  uint64_t* tx_ok = bars + 31;     // [2] the peer has read the tile we copied into it (1 remote arrival)
-  uint64_t* q_full = bars + 33;    // Q_r is in TMEM (128 arrivals)
-  uint64_t* drain = bars + 34;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 35);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 36);
+  uint64_t* staged = bars + 26;    // [2] partial scores of a unit are in sStg (128 arrivals)
+  uint64_t* rx_read = bars + 28;   // [2] this CTA has read a receive buffer (128 arrivals)
+  uint64_t* rx_full = bars + 30;   // [2] the peer's partial scores are in sRx (armed with expect_tx)
+  uint64_t* tx_ok = bars + 32;     // [2] the peer has read the unit we copied into it (1 remote arrival)
+  uint64_t* q_full = bars + 34;    // Q_r is in TMEM and shared memory (128 arrivals)
+  uint64_t* drain = bars + 35;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 36);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 37);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
@@ -217,14 +228,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     }
     return;
   }
-  const int n_tiles = (t1 - t0 + kMlaTile - 1) / kMlaTile;
+  const int n_units = (t1 - t0 + kMlaUnit - 1) / kMlaUnit;
+  const int n_tiles = (n_units + 1) / 2;
   const int n_pages = (L + p.bs - 1) / p.bs;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 35; ++i) mbar_init(&bars[i], (i >= 19 && i <= 21) || (i >= 25 && i <= 28) || i == 33 ? 128 : 1);
+    for (int i = 0; i < 36; ++i)
+      mbar_init(&bars[i], (i >= 18 && i <= 21) || (i >= 26 && i <= 29) || i == 34 ? 128 : 1);
     *abort_flag = 0;
     fence_barrier_init();
-    // arm the receive buffers for tiles 0 and 1
+    // arm the receive buffers for units 0 and 1
     mbar_arrive_expect_tx(&rx_full[0], Sh::kRxBuf);
     mbar_arrive_expect_tx(&rx_full[1], Sh::kRxBuf);
   }
@@ -238,7 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // A wait that also gives up when another role has aborted.  Cluster-scope
-  // acquire so that the peer's DSMEM writes released by its arrivals are visible.
+  // acquire, which also covers the peer's arrivals on this CTA's barriers.
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t ts = global_timer_ns();
@@ -257,21 +270,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
-    // Per tile and page piece: lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3,
+    // Per unit and page piece: lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3,
     // lane 5 pi + 4 the rope half block 512 + 32 r .. + 31.
     const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
     if (lane == 0) {
       tma_prefetch_desc(&tmKV);
       tma_prefetch_desc(&tmKVh);
     }
-    const int R = min(p.bs, kMlaTile);  // rows per box
-    const int pieces = kMlaTile / R;
+    const int R = min(p.bs, kMlaUnit);  // rows per box
+    const int pieces = kMlaUnit / R;
     const int pi = lane / 5, lb = lane - pi * 5;
     const uint64_t pol = l2_policy_evict_first();
     int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % kMlaStages;
-      const int tok = t0 + j * kMlaTile + pi * R;
+    for (int u = 0; u < n_units; ++u) {
+      const int st = u % kMlaStages;
+      const int tok = t0 + u * kMlaUnit + pi * R;
       const int pg = tok / p.bs;
       const bool live = pi < pieces && pg < n_pages;
       int rowc = 0;
@@ -280,93 +293,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         rowc = b < 0 ? -R : b * p.bs + (tok - pg * p.bs);
       }
       const uint32_t n_live = (uint32_t)__popc(__ballot_sync(0xffffffffu, live && lb == 0));
-      if (j >= kMlaStages && !wait_all(&kv_empty[st], ((j / kMlaStages) - 1) & 1)) break;
+      if (u >= kMlaStages && !wait_all(&kv_empty[st], ((u / kMlaStages) - 1) & 1)) break;
       if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], n_live * (uint32_t)(R * (4 * 128 + 64)));
       __syncwarp();
       if (live) {
-        uint8_t* dst = sKV + st * Sh::kStage;
         if (lb < 4)
-          tma_load_3d(dst + lb * Sh::kBlk + pi * R * 128, &tmKV, &kv_full[st], (4 * (int)rank + lb) * 64, 0, rowc,
-                      pol);
+          tma_load_3d(sKV + (lb * kMlaStages + st) * Sh::kBlk + pi * R * 128, &tmKV, &kv_full[st],
+                      (4 * (int)rank + lb) * 64, 0, rowc, pol);
         else
-          tma_load_3d(dst + 4 * Sh::kBlk + pi * R * 64, &tmKVh, &kv_full[st], kMlaDv + 32 * (int)rank, 0, rowc, pol);
+          tma_load_3d(sRope + st * Sh::kRopeU + pi * R * 64, &tmKVh, &kv_full[st], kMlaDv + 32 * (int)rank, 0, rowc,
+                      pol);
       }
       ++issued;
     }
     if (*abort_flag)
-      for (int j = max(0, issued - kMlaStages); j < issued; ++j)
-        mbar_wait(&kv_full[j % kMlaStages], (j / kMlaStages) & 1, &g_status_mla);
+      for (int u = max(0, issued - kMlaStages); u < issued; ++u)
+        mbar_wait(&kv_full[u % kMlaStages], (u / kMlaStages) & 1, &g_status_mla);
   } else if (warp == 5) {
     // ------------------------------------------------------------ UMMA issuer
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kMlaRows, kMlaTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kMlaRows, kMlaHalf, false, true);
+    const uint32_t kv = smem_u32(sKV), rope = smem_u32(sRope), qr = smem_u32(sQr);
     bool issued = false;
-    auto qk = [&](int j) {  // partial S_j = Q_r K_r^T over this CTA's 288 key dimensions
+    auto qk = [&](int j) {  // partial S_j = Q_r K_r^T over this CTA's 288 key dimensions, 64 tokens
       if (lane == 0) {
-        const uint32_t kb = smem_u32(sKV + (j % kMlaStages) * Sh::kStage);
-        const uint32_t d_tmem = tmem + kTmS + (j % kMlaSBufs) * kMlaTile;
+        const int s0 = (2 * j) % kMlaStages;
+        const uint32_t d_tmem = tmem + kTmS + (j & 1) * kMlaTile;
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
           umma_bf16_tmem_a(d_tmem, tmem + kTmQ + kk * 8,
-                           umma_desc_sw128(kb + (kk >> 2) * Sh::kBlk + (kk & 3) * 32, 16, 1024), kIdQK,
-                           kk > 0 ? 1u : 0u);
+                           umma_desc_sw128(kv + ((kk >> 2) * kMlaStages + s0) * Sh::kBlk + (kk & 3) * 32, 16, 1024),
+                           kIdQK, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
-          umma_bf16_tmem_a(d_tmem, tmem + kTmQ + 128 + kk * 8, umma_desc_sw64(kb + 4 * Sh::kBlk + kk * 32, 512), kIdQK,
-                           1u);
-        umma_commit(&s_full[j % kMlaSBufs]);
+          umma_bf16(d_tmem, umma_desc_sw64(qr + kk * 32, 512), umma_desc_sw64(rope + s0 * Sh::kRopeU + kk * 32, 512),
+                    kIdQK, 1u);
+        umma_commit(&s_full[j & 1]);
       }
+    };
+    auto wait_tile = [&](int j) -> bool {  // the latent units of tile j have landed
+      const int u0 = 2 * j;
+      if (!wait_all(&kv_full[u0 % kMlaStages], (u0 / kMlaStages) & 1)) return false;
+      if (u0 + 1 < n_units && !wait_all(&kv_full[(u0 + 1) % kMlaStages], ((u0 + 1) / kMlaStages) & 1)) return false;
+      tc_fence_after_sync();
+      return true;
     };
     bool ok = wait_all(q_full, 0);
     if (ok) tc_fence_after_sync();
-    for (int j = 0; ok && j < kMlaSBufs && j < n_tiles; ++j) {
-      if (!wait_all(&kv_full[j % kMlaStages], (j / kMlaStages) & 1)) {
+    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
+      if (!wait_tile(j)) {
         ok = false;
         break;
       }
-      tc_fence_after_sync();
       qk(j);
       issued = true;
       __syncwarp();
     }
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int st = j % kMlaStages, sb = j % kMlaSBufs;
-      if (!wait_all(&p_full[sb], (j / kMlaSBufs) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const int tok0 = t0 + j * kMlaTile;
-      if (tok0 + kMlaTile > t1) {
-        // rows past the partition end (NaN tails, pieces not loaded): zero the value columns
-        uint8_t* vb = sKV + st * Sh::kStage;
-        for (int row = (t1 - tok0) + lane; row < kMlaTile; row += 32)
-          for (int b = 0; b < 4; ++b) {
-            uint4* d = reinterpret_cast<uint4*>(vb + b * Sh::kBlk + row * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      if (lane == 0) {
-        const uint32_t vbase = smem_u32(sKV + st * Sh::kStage);
-#pragma unroll
-        for (int kk = 0; kk < kMlaTile / 16; ++kk)
-          umma_bf16_tmem_a(tmem + kTmO, tmem + kTmS + sb * kMlaTile + kk * 8,
-                           umma_desc_sw128(vbase + kk * 2048, Sh::kBlk, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[sb]);
-        umma_commit(&kv_empty[st]);
-      }
-      __syncwarp();
-      const int jn = j + kMlaSBufs;  // QK_jn overwrites S[sb] after PV_j (in issue order)
-      if (jn < n_tiles) {
-        if (!wait_all(&kv_full[jn % kMlaStages], (jn / kMlaStages) & 1)) {
+      for (int h = 0; ok && h < 2; ++h) {
+        const int u = 2 * j + h;
+        if (u >= n_units) break;
+        if (!wait_all(&p_full[u % 4], (u / 4) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        qk(jn);
+        const int st = u % kMlaStages;
+        const int tok0 = t0 + u * kMlaUnit;
+        if (tok0 + kMlaUnit > t1) {
+          // rows past the partition end (NaN tails, pieces not loaded): zero the value columns
+          for (int row = (t1 - tok0) + lane; row < kMlaUnit; row += 32)
+            for (int b = 0; b < 4; ++b) {
+              uint4* d = reinterpret_cast<uint4*>(sKV + (b * kMlaStages + st) * Sh::kBlk + row * 128);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kMlaUnit / 16; ++kk)
+            umma_bf16_tmem_a(tmem + kTmO, tmem + kTmS + (j & 1) * kMlaTile + h * 16 + kk * 8,
+                             umma_desc_sw128(kv + st * Sh::kBlk + kk * 2048, kMlaStages * Sh::kBlk, 1024), kIdPV,
+                             (u > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&pv_done[u % 4]);
+          umma_commit(&kv_empty[st]);
+        }
+        __syncwarp();
+      }
+      if (ok && j + 2 < n_tiles) {  // QK_{j+2} overwrites S[j & 1] after P V of tile j (in issue order)
+        if (!wait_tile(j + 2)) {
+          ok = false;
+          break;
+        }
+        qk(j + 2);
         __syncwarp();
       }
     }
@@ -380,16 +401,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const uint32_t peer_rx = dsmem_map(smem_u32(sRx), peer);
     const uint32_t peer_rx_full = dsmem_map(smem_u32(rx_full), peer);
     const uint32_t peer_tx_ok = dsmem_map(smem_u32(tx_ok), peer);
-    for (int t = 0; t <= n_tiles; ++t) {
-      if (t < n_tiles) {  // staged tile t -> the peer's receive buffer t & 1
+    for (int t = 0; t <= n_units; ++t) {
+      if (t < n_units) {  // staged unit t -> the peer's receive buffer t & 1
         const int b = t & 1;
         if (!wait_all(&staged[b], (t >> 1) & 1)) break;
         if (lane == 0)
           bulk_copy_to_peer(peer_rx + b * Sh::kRxBuf, smem_u32(sStg) + b * Sh::kRxBuf, Sh::kRxBuf, peer_rx_full + b * 8);
         __syncwarp();
       }
-      const int u = t - 1;  // credit: this CTA has read tile u, so the peer may send tile u + 2
-      if (u >= 0 && u + 2 < n_tiles) {
+      const int u = t - 1;  // credit: this CTA has read unit u, so the peer may send unit u + 2
+      if (u >= 0 && u + 2 < n_units) {
         const int b = u & 1;
         if (!wait_all(&rx_read[b], (u >> 1) & 1)) break;
         // Relaxed: the only thing the credit must order is the softmax threads' reads
@@ -407,8 +428,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const bool row_valid = row < p.hrows && head < p.H;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     {
-      // Q_r of this head into TMEM columns kTmQ.. as bf16 pairs (the raw row words):
-      // latent dims 256 r .. 256 r + 255, then rope dims 512 + 32 r .. + 31.
+      // Q_r of this head: latent dims 256 r .. 256 r + 255 into TMEM columns kTmQ..
+      // as bf16 pairs (the raw row words); rope dims 512 + 32 r .. + 31 into row
+      // `row` of the 64-byte-swizzled shared tile (16-byte chunk c at c ^ ((row >> 1) & 3)).
       const uint4* src = p.q + ((size_t)s * p.H + (row_valid ? head : 0)) * (kMlaDq / 8);
       uint32_t qa[64];
 #pragma unroll
@@ -416,18 +438,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         const uint4 v = row_valid ? __ldg(src + 32 * rank + i) : make_uint4(0u, 0u, 0u, 0u);
         qa[4 * i] = v.x, qa[4 * i + 1] = v.y, qa[4 * i + 2] = v.z, qa[4 * i + 3] = v.w;
       }
-      uint32_t qb[80];
+      uint32_t qb[64];
 #pragma unroll
-      for (int i = 0; i < 20; ++i) {
-        const int idx = i < 16 ? 32 * rank + 16 + i : kMlaDv / 8 + 4 * rank + (i - 16);
-        const uint4 v = row_valid ? __ldg(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < 16; ++i) {
+        const uint4 v = row_valid ? __ldg(src + 32 * rank + 16 + i) : make_uint4(0u, 0u, 0u, 0u);
         qb[4 * i] = v.x, qb[4 * i + 1] = v.y, qb[4 * i + 2] = v.z, qb[4 * i + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = row_valid ? __ldg(src + kMlaDv / 8 + 4 * rank + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sQr + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = v;
       }
       tmem_st32(lane_base + kTmQ, qa);
       tmem_st32(lane_base + kTmQ + 32, qa + 32);
       tmem_st32(lane_base + kTmQ + 64, qb);
       tmem_st32(lane_base + kTmQ + 96, qb + 32);
-      tmem_st16(lane_base + kTmQ + 128, qb + 64);
+      fence_proxy_async_smem();  // the score UMMA reads the rope tile through the async proxy
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(q_full);
@@ -438,45 +464,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     // staging / receive rows of this head: 8 chunks of 4 floats, chunk c stored at
     // c ^ (row & 7) so that the 8 rows a quarter-warp touches hit distinct banks
     const int rsw = row & 7;
-    float* my_stg = sStg + row * kMlaTile;
-    const float* my_rx = sRx + row * kMlaTile;
-    auto load_s = [&](int t, uint32_t* v) -> bool {  // this CTA's partial scores of tile t
-      if (!wait_all(&s_full[t % kMlaSBufs], (t / kMlaSBufs) & 1)) return false;
-      tc_fence_after_sync();
-      tmem_ld32(lane_base + kTmS + (t % kMlaSBufs) * kMlaTile, v);
+    float* my_stg = sStg + row * kMlaUnit;
+    const float* my_rx = sRx + row * kMlaUnit;
+    auto load_s = [&](int u, uint32_t* v) -> bool {  // this CTA's partial scores of unit u
+      const int j = u >> 1;
+      if ((u & 1) == 0) {
+        if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) return false;
+        tc_fence_after_sync();
+      }
+      tmem_ld32(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * kMlaUnit, v);
       tmem_ld_wait();
       return true;
     };
-    auto stage = [&](int t, const uint32_t* v) -> bool {  // into staging buffer t & 1 for the exchange warp
-      const int b = t & 1;
-      // the copy of tile t - 2 out of this buffer has landed (the peer has even read it)
-      if (t >= 2 && !wait_all(&tx_ok[b], ((t >> 1) - 1) & 1)) return false;
+    auto stage = [&](int u, const uint32_t* v) -> bool {  // into staging buffer u & 1 for the exchange warp
+      const int b = u & 1;
+      // the copy of unit u - 2 out of this buffer has landed (the peer has even read it)
+      if (u >= 2 && !wait_all(&tx_ok[b], ((u >> 1) - 1) & 1)) return false;
       float* dst = my_stg + b * (Sh::kRxBuf / 4);
 #pragma unroll
-      for (int c = 0; c < kMlaTile / 4; ++c)
+      for (int c = 0; c < kMlaUnit / 4; ++c)
         *reinterpret_cast<uint4*>(dst + ((c ^ rsw) << 2)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       fence_proxy_async_smem();  // the bulk copy reads through the async proxy
       mbar_arrive(&staged[b]);
       return true;
     };
-    uint32_t cur[kMlaTile], nxt[kMlaTile];
-    int armed0 = 0, armed1 = n_tiles > 1 ? 1 : -1;  // newest tile each receive buffer is armed for (thread 0)
+    uint32_t cur[kMlaUnit], nxt[kMlaUnit];
+    int armed0 = 0, armed1 = n_units > 1 ? 1 : -1;  // newest unit each receive buffer is armed for (thread 0)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = load_s(0, cur) && stage(0, cur);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (j + 1 < n_tiles && !(load_s(j + 1, nxt) && stage(j + 1, nxt))) {
+    for (int u = 0; ok && u < n_units; ++u) {
+      if (u + 1 < n_units && !(load_s(u + 1, nxt) && stage(u + 1, nxt))) {
         ok = false;
         break;
       }
-      const int b = j & 1, sb = j % kMlaSBufs;
-      if (!wait_all(&rx_full[b], (j >> 1) & 1)) {
+      const int b = u & 1, j = u >> 1;
+      if (!wait_all(&rx_full[b], (u >> 1) & 1)) {
         ok = false;
         break;
       }
-      float sc[kMlaTile];
+      float sc[kMlaUnit];
       const float* rx = my_rx + b * (Sh::kRxBuf / 4);
 #pragma unroll
-      for (int c = 0; c < kMlaTile / 4; ++c) {
+      for (int c = 0; c < kMlaUnit / 4; ++c) {
         const float4 v = *reinterpret_cast<const float4*>(rx + ((c ^ rsw) << 2));
         sc[4 * c] = __uint_as_float(cur[4 * c]) + v.x;
         sc[4 * c + 1] = __uint_as_float(cur[4 * c + 1]) + v.y;
@@ -484,19 +513,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         sc[4 * c + 3] = __uint_as_float(cur[4 * c + 3]) + v.w;
       }
       mbar_arrive(&rx_read[b]);
-      // re-arm buffer b for tile j + 2: its data cannot arrive before every thread here
-      // has read tile j (the peer waits for the credit that rx_read leads to)
-      if (threadIdx.x == 0 && j + 2 < n_tiles) {
+      // re-arm buffer b for unit u + 2: its data cannot arrive before every thread here
+      // has read unit u (the peer waits for the credit that rx_read leads to)
+      if (threadIdx.x == 0 && u + 2 < n_units) {
         mbar_arrive_expect_tx(&rx_full[b], Sh::kRxBuf);
-        if (b) armed1 = j + 2;
-        else armed0 = j + 2;
+        if (b) armed1 = u + 2;
+        else armed0 = u + 2;
       }
-      const int vis = min(kMlaTile, t1 - (t0 + j * kMlaTile));
+      const int vis = min(kMlaUnit, t1 - (t0 + u * kMlaUnit));
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kMlaTile; ++c) mx[c & 7] = fmaxf(mx[c & 7], c < vis ? sc[c] * sgn : -INFINITY);
+      for (int c = 0; c < kMlaUnit; ++c) mx[c & 7] = fmaxf(mx[c & 7], c < vis ? sc[c] * sgn : -INFINITY);
       const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
       const bool grow = m_new > m_run + 8.0f;
@@ -505,9 +534,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         alpha = exp2_approx(m_run - m_new);
         m_run = m_new;
       }
-      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-        // O_r holds PV_{j-1} only once that UMMA completed (PV_j is not issued yet)
-        if (!wait_all(&pv_done[(j - 1) % kMlaSBufs], ((j - 1) / kMlaSBufs) & 1)) {
+      if (u >= 1 && __any_sync(0xffffffffu, grow)) {
+        // O_r holds every earlier unit only once P V of unit u - 1 completed
+        if (!wait_all(&pv_done[(u - 1) % 4], ((u - 1) / 4) & 1)) {
           ok = false;
           break;
         }
@@ -527,9 +556,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       float ls[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-      uint32_t pk[kMlaTile / 2];
+      uint32_t pk[kMlaUnit / 2];
 #pragma unroll
-      for (int c = 0; c < kMlaTile; c += 2) {
+      for (int c = 0; c < kMlaUnit; c += 2) {
         const float e0 = c < vis ? exp2_approx(fmaf(sc[c] * sgn, asl2, neg_m)) : 0.f;
         const float e1 = c + 1 < vis ? exp2_approx(fmaf(sc[c + 1] * sgn, asl2, neg_m)) : 0.f;
         ls[c & 7] += e0;
@@ -537,14 +566,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         pk[c >> 1] = pack_bf16x2(e0, e1);
       }
       l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tmem_st16(lane_base + kTmS + sb * kMlaTile, pk);
+      tmem_st16(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * 16, pk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[u % 4]);
 #pragma unroll
-      for (int c = 0; c < kMlaTile; ++c) cur[c] = nxt[c];
+      for (int c = 0; c < kMlaUnit; ++c) cur[c] = nxt[c];
     }
-    if (ok && wait_all(&pv_done[(n_tiles - 1) % kMlaSBufs], ((n_tiles - 1) / kMlaSBufs) & 1)) {
+    if (ok && wait_all(&pv_done[(n_units - 1) % 4], ((n_units - 1) / 4) & 1)) {
       tc_fence_after_sync();
       const float inv = 1.0f / l_run;
       const size_t sh = (size_t)s * p.H + head;
@@ -663,7 +692,7 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   if (num_seqs > 65535) return fail(METIS_E_SHAPE, "num_seqs must be <= 65535");
   if ((long long)max_blocks * block_size > 0x7fffffffLL || (long long)num_blocks * block_size > 0x7fffffffLL)
     return fail(METIS_E_SHAPE, "max_blocks * block_size and num_blocks * block_size must fit in int32");
-  if (partition_size < 0 || partition_size % kMlaTile)
+  if (partition_size < 0 || partition_size % kMlaUnit)
     return fail(METIS_E_SHAPE, "partition_size must be 0 or a positive multiple of 32");
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
       !aligned(seq_lens, 4) || !aligned(lse_out, 4))
@@ -704,11 +733,11 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   CUtensorMap tmKV, tmKVh;
   const uint64_t kdims[3] = {(uint64_t)kMlaDq, 1, (uint64_t)num_blocks * block_size};
   const uint64_t kstr[2] = {(uint64_t)kMlaDq * 2, (uint64_t)kMlaDq * 2};
-  const uint32_t kbox[3] = {64, 1, (uint32_t)std::min(block_size, kMlaTile)};
+  const uint32_t kbox[3] = {64, 1, (uint32_t)std::min(block_size, kMlaUnit)};
   int rc = encode_tiled(&tmKV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, kbox,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  const uint32_t khbox[3] = {32, 1, (uint32_t)std::min(block_size, kMlaTile)};
+  const uint32_t khbox[3] = {32, 1, (uint32_t)std::min(block_size, kMlaUnit)};
   rc = encode_tiled(&tmKVh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, khbox,
                     CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
