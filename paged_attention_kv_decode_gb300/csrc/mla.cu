@@ -9,43 +9,47 @@
 // arrive already in latent space (the absorbed up-projection is upstream).
 //
 // Decomposition.  A (sequence, partition) is computed by a CLUSTER OF TWO CTAs
-// (two SMs) that split both contractions, so no product is computed twice and
-// every latent byte is read by exactly one of them:
+// (two SMs); nothing is computed twice and every latent byte is read once:
 //   * scores: CTA r owns the key dimensions D_r = [256 r, 256 r + 256) of the
-//     latent part plus [512 + 32 r, 512 + 32 r + 32) of the rope part.  It
-//     computes the partial S_r = Q[:, D_r] K[:, D_r]^T and sends it (fp32) into
-//     its peer's shared memory (DSMEM); both add S_0 + S_1 in the same order, so
-//     both see bit-identical softmax weights;
+//     latent part plus [512 + 32 r, 512 + 32 r + 32) of the rope part and
+//     computes the partial S_r = Q[:, D_r] K[:, D_r]^T for all 128 heads;
+//   * softmax: CTA r owns heads [64 r, 64 r + 64).  It sends its partial scores
+//     of the other 64 heads to the peer and receives the peer's partial of its
+//     own heads (fp32, through distributed shared memory), runs the online
+//     softmax of its heads, and sends P of its heads (bf16) plus their rescale
+//     factors back, so both CTAs hold P of all heads;
 //   * output: CTA r owns output columns [256 r, 256 r + 256) (O_r in TMEM), whose
 //     values are exactly the latent columns it already loads for its keys.
 //
-// Granularity.  A UMMA costs at least ~46 cycles whatever its N, so N = 32
-// wastes two thirds of the tensor pipe: the scores are computed for 64-token
-// tiles (N = 64).  Softmax, the score exchange and P V run on 32-token units,
-// two per tile.  Per CTA and unit that is 18 KB of latent (four
-// 128-byte-swizzled 64-column blocks plus one 64-byte-swizzled 32-column rope
-// half block), streamed through an 8-unit TMA ring laid out block-major, so
-// that the two units of a tile are one contiguous 64-row operand per block.
+// Granularity.  A UMMA costs at least ~46 cycles whatever its N, so the scores
+// are computed for 64-token tiles (N = 64); the exchange, the softmax and P V run
+// on 32-token units, two per tile.  Per CTA and unit that is 18 KB of latent
+// (four 128-byte-swizzled 64-column blocks plus one 64-byte-swizzled 32-column
+// rope half block), streamed through an 8-unit TMA ring laid out block-major so
+// that the two units of a tile form one 64-row operand per block.
 //
-// TMEM (512 columns): O_r 256 | S 2 x 64 (P of a unit is written back over the
-// scores as bf16 pairs) | the latent part of Q_r, 128 columns of bf16 pairs (the
-// A operand of the score UMMA).  The rope part of Q_r (32 dimensions) sits in
-// shared memory.
+// TMEM (512 columns): O_r 256 | S 2 x 64 | the latent part of Q_r as bf16 pairs,
+// 128 (the A operand of the score UMMA).  The rope part of Q_r and the P tiles
+// (the A operand of P V) sit in shared memory, so a score buffer is free as soon
+// as it has been read and the next scores never wait for P V.
 //
-//   warp 4       TMA producer (latent units)
-//   warp 5       TMEM allocation; one lane issues the UMMAs:
-//                  S_r = Q_r K_r^T   (M 128 heads, N 64 tokens, K 288)
-//                  O_r += P V_r      (M 128, N 256, K 32 per unit; P from TMEM)
-//   warp 6       exchange: one bulk copy per unit moves the staged partial
-//                scores into the peer's receive buffer (completing on the peer's
-//                mbarrier), and returns the credit once this CTA has read a
-//                receive buffer.  Every remote operation is on this warp, off
-//                the softmax path.
-//   warps 0..3   one head (TMEM lane) per thread: Q_r into TMEM / shared memory;
-//                then per unit stage this head's partial scores of the NEXT unit
-//                (so the exchange overlaps a softmax), add the peer's partial of
-//                this unit, online softmax in log2 units (O rescaled in TMEM only
-//                when the max grows past 2^8), P back into TMEM; epilogue O_r / l
+// Head order.  TMEM lane L = 32 q + 16 g + i (quarter q, half g, i < 16) holds
+// head 64 g + 16 q + i of the head tile, so every lane quarter -- and with it
+// every SM sub-partition, since warp w may only touch quarter w % 4 -- holds 16
+// heads of each CTA: the softmax work is spread over all four sub-partitions.
+//
+// Warps:
+//   0-3   row warps (quarter = warp): stage the partial scores of the peer's 16
+//         heads of the quarter one unit ahead; softmax of its own 16 heads with
+//         two lanes per head (lane i and i ^ 16, 16 tokens each; row maxima and
+//         sums combined by shuffles); write P and the rescale factors; epilogue
+//   4-7   rescale warps (quarter = warp - 4): once P of a unit is complete in
+//         both CTAs, apply its rescale factors (own and peer heads) to O in TMEM
+//   8     TMA producer          9    TMEM allocation + UMMA issue
+//   10    score exchange: bulk copy staged partials to the peer, credit the peer
+//         once a receive buffer has been read
+//   11    P exchange: bulk copy P rows of own heads (+ factors) to the peer,
+//         credit the peer once P V has released a P slot; final row statistics
 //
 // A schedule kernel lists the (sequence, partition) work items heaviest first.
 // A sequence with one partition writes its output directly; longer ones write
@@ -67,27 +71,34 @@ __device__ unsigned int g_status_mla = 0;
 constexpr int kMlaDq = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaHalf = 256;       // output columns (and latent key columns) per CTA
-constexpr int kMlaUnit = 32;        // tokens per softmax / exchange / P V unit and per ring stage
+constexpr int kMlaUnit = 32;        // tokens per exchange / softmax / P V unit and per ring stage
 constexpr int kMlaTile = 64;        // tokens per score UMMA (two units)
-constexpr int kMlaRows = 128;       // heads per CTA (the UMMA M)
-constexpr int kMlaThreads = 224;    // 4 softmax warps + TMA warp + MMA warp + exchange warp
+constexpr int kMlaRows = 128;       // heads per head tile (the UMMA M)
+constexpr int kMlaOwn = 64;         // heads whose softmax a CTA runs
+constexpr int kMlaThreads = 384;    // 12 warps
 constexpr int kMlaTmemCols = 512;
 constexpr int kMlaSortMax = 2048;
 constexpr int kMlaStages = 8;       // ring stages of one unit (even: a tile is two adjacent stages)
+constexpr int kMlaNX = 2;           // partial-score exchange slots
+constexpr int kMlaNP = 3;           // P tile slots
 constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
-constexpr uint32_t kTmS = 256;      // 2 x 64 columns: S, then P (bf16 pairs, 16 columns per unit)
+constexpr uint32_t kTmS = 256;      // 2 x 64 columns: partial scores of a tile
 constexpr uint32_t kTmQ = 384;      // 128 columns: latent part of Q_r as bf16 pairs
 
 struct MlaShape {
   static constexpr int kBlk = kMlaUnit * 128;             // one unit of one 64-column block (128-byte swizzle)
   static constexpr int kRopeU = kMlaUnit * 64;            // one unit of the rope half block (64-byte swizzle)
-  static constexpr int kRxBuf = kMlaRows * kMlaUnit * 4;  // one unit of partial scores, fp32
+  static constexpr int kXBuf = kMlaOwn * kMlaUnit * 4;    // partial scores of 64 heads x one unit, fp32
+  static constexpr int kPBuf = kMlaRows * kMlaUnit * 2;   // P of 128 lanes x one unit, bf16, 64-byte swizzle
   static constexpr int kKv = 0;                           // block b of stage s at kKv + (b * kMlaStages + s) * kBlk
   static constexpr int kRope = kKv + 4 * kMlaStages * kBlk;  // stage s at kRope + s * kRopeU
-  static constexpr int kQr = kRope + kMlaStages * kRopeU;    // rope part of Q_r: 128 rows x 64 B, 64-byte swizzle
-  static constexpr int kRx = kQr + kMlaRows * 64;         // two receive buffers (written by the peer)
-  static constexpr int kStg = kRx + 2 * kRxBuf;           // two staging buffers (copied to the peer)
-  static constexpr int kBars = kStg + 2 * kRxBuf;         // 216 KB, then the barriers
+  static constexpr int kQr = kRope + kMlaStages * kRopeU;    // rope part of Q_r: 128 lanes x 64 B, 64-byte swizzle
+  static constexpr int kStg = kQr + kMlaRows * 64;        // kMlaNX staging buffers (copied to the peer)
+  static constexpr int kRx = kStg + kMlaNX * kXBuf;       // kMlaNX receive buffers (written by the peer)
+  static constexpr int kP = kRx + kMlaNX * kXBuf;         // kMlaNP P tiles
+  static constexpr int kAlpha = kP + kMlaNP * kPBuf;      // kMlaNP x 128 rescale factors (head order)
+  static constexpr int kStat = kAlpha + kMlaNP * kMlaRows * 4;  // 128 x {m, l} (head order)
+  static constexpr int kBars = kStat + kMlaRows * 8;
   static constexpr int kSmem = kBars + 512 + 1024;        // + alignment slack
 };
 
@@ -171,26 +182,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   uint8_t* sKV = smem + Sh::kKv;
   uint8_t* sRope = smem + Sh::kRope;
   uint8_t* sQr = smem + Sh::kQr;
-  float* sRx = reinterpret_cast<float*>(smem + Sh::kRx);
-  float* sStg = reinterpret_cast<float*>(smem + Sh::kStg);
+  uint8_t* sStg = smem + Sh::kStg;
+  uint8_t* sRx = smem + Sh::kRx;
+  uint8_t* sP = smem + Sh::kP;
+  float* sAlpha = reinterpret_cast<float*>(smem + Sh::kAlpha);
+  float* sStat = reinterpret_cast<float*>(smem + Sh::kStat);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBars);
-  uint64_t* kv_full = bars + 0;    // [kMlaStages]
-  uint64_t* kv_empty = bars + 8;   // [kMlaStages]
-  uint64_t* s_full = bars + 16;    // [2] scores of tile j landed in S[j & 1]
-  // [4] P of unit u written (128 arrivals) / P V of unit u completed, on barrier u % 4:
-  // at most three P V units are outstanding while unit u is processed, and the
-  // softmax never runs four units ahead of the UMMA issuer, so parity waits on
-  // these are unambiguous
-  uint64_t* p_full = bars + 18;
-  uint64_t* pv_done = bars + 22;
-  uint64_t* staged = bars + 26;    // [2] partial scores of a unit are in sStg (128 arrivals)
-  uint64_t* rx_read = bars + 28;   // [2] this CTA has read a receive buffer (128 arrivals)
-  uint64_t* rx_full = bars + 30;   // [2] the peer's partial scores are in sRx (armed with expect_tx)
-  uint64_t* tx_ok = bars + 32;     // [2] the peer has read the unit we copied into it (1 remote arrival)
-  uint64_t* q_full = bars + 34;    // Q_r is in TMEM and shared memory (128 arrivals)
-  uint64_t* drain = bars + 35;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 36);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 37);
+  uint64_t* kv_full = bars + 0;     // [kMlaStages]
+  uint64_t* kv_empty = bars + 8;    // [kMlaStages]
+  uint64_t* s_full = bars + 16;     // [2] partial scores of tile j in S[j & 1]
+  uint64_t* pv_done = bars + 18;    // [4] P V of unit u completed, on u % 4
+  uint64_t* staged = bars + 22;     // [kMlaNX] partial scores of the peer's heads staged (128 arrivals)
+  uint64_t* rx_full = bars + 24;    // [kMlaNX] the peer's partial of own heads landed (armed with expect_tx)
+  uint64_t* rx_read = bars + 26;    // [kMlaNX] a receive buffer has been read (128 arrivals)
+  uint64_t* tx_ok = bars + 28;      // [kMlaNX] credit from the peer: it has read what we sent (remote)
+  uint64_t* p_local = bars + 30;    // [kMlaNP] P of own heads + factors written (128 arrivals)
+  uint64_t* p_remote = bars + 33;   // [kMlaNP] P of the peer's heads + factors landed (armed with expect_tx)
+  uint64_t* p_relay = bars + 36;    // [kMlaNP] O rescaled for the unit, P complete (128 arrivals)
+  uint64_t* pslot_ok = bars + 39;   // [kMlaNP] credit from the peer: its P slot is free (remote)
+  uint64_t* q_full = bars + 42;     // Q_r in TMEM / shared memory (128 arrivals)
+  uint64_t* stat_local = bars + 43; // final statistics of own heads written (128 arrivals)
+  uint64_t* stat_full = bars + 44;  // final statistics of the peer's heads landed (armed with expect_tx)
+  uint64_t* drain = bars + 45;
+  uint64_t* s_free = bars + 46;     // [2] the row warps have read S[j & 1] of tile j (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 48);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 49);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
@@ -231,17 +247,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const int n_units = (t1 - t0 + kMlaUnit - 1) / kMlaUnit;
   const int n_tiles = (n_units + 1) / 2;
   const int n_pages = (L + p.bs - 1) / p.bs;
+  constexpr uint32_t kPHalfBytes = kMlaOwn * 64 + kMlaOwn * 4;  // P rows + factors of 64 heads
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 36; ++i)
-      mbar_init(&bars[i], (i >= 18 && i <= 21) || (i >= 26 && i <= 29) || i == 34 ? 128 : 1);
+    for (int i = 0; i < 48; ++i) {
+      const bool many = (i >= 22 && i <= 23) || (i >= 26 && i <= 27) || (i >= 30 && i <= 32) || (i >= 36 && i <= 38) ||
+                        i == 42 || i == 43 || i == 46 || i == 47;
+      mbar_init(&bars[i], many ? 128 : 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
-    // arm the receive buffers for units 0 and 1
-    mbar_arrive_expect_tx(&rx_full[0], Sh::kRxBuf);
-    mbar_arrive_expect_tx(&rx_full[1], Sh::kRxBuf);
+    // arm the receive slots for the first units and the final statistics
+    for (int x = 0; x < kMlaNX; ++x) mbar_arrive_expect_tx(&rx_full[x], Sh::kXBuf);
+    for (int x = 0; x < kMlaNP; ++x) mbar_arrive_expect_tx(&p_remote[x], kPHalfBytes);
+    mbar_arrive_expect_tx(stat_full, kMlaOwn * 8);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kMlaTmemCols);
     tmem_relinquish();
   }
@@ -268,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   };
   auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     // Per unit and page piece: lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3,
     // lane 5 pi + 4 the rope half block 512 + 32 r .. + 31.
@@ -309,11 +330,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     if (*abort_flag)
       for (int u = max(0, issued - kMlaStages); u < issued; ++u)
         mbar_wait(&kv_full[u % kMlaStages], (u / kMlaStages) & 1, &g_status_mla);
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ UMMA issuer
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kMlaRows, kMlaTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kMlaRows, kMlaHalf, false, true);
-    const uint32_t kv = smem_u32(sKV), rope = smem_u32(sRope), qr = smem_u32(sQr);
+    const uint32_t kv = smem_u32(sKV), rope = smem_u32(sRope), qr = smem_u32(sQr), pt = smem_u32(sP);
     bool issued = false;
     auto qk = [&](int j) {  // partial S_j = Q_r K_r^T over this CTA's 288 key dimensions, 64 tokens
       if (lane == 0) {
@@ -350,10 +371,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       __syncwarp();
     }
     for (int j = 0; ok && j < n_tiles; ++j) {
+      if (j + 2 < n_tiles) {  // QK_{j+2} into S[j & 1] once the row warps have read tile j
+        if (!wait_all(&s_free[j & 1], (j >> 1) & 1) || !wait_tile(j + 2)) {
+          ok = false;
+          break;
+        }
+        qk(j + 2);
+        __syncwarp();
+      }
       for (int h = 0; ok && h < 2; ++h) {
         const int u = 2 * j + h;
         if (u >= n_units) break;
-        if (!wait_all(&p_full[u % 4], (u / 4) & 1)) {
+        const int x = u % kMlaNP;
+        if (!wait_all(&p_relay[x], (u / kMlaNP) & 1)) {
           ok = false;
           break;
         }
@@ -374,20 +404,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < kMlaUnit / 16; ++kk)
-            umma_bf16_tmem_a(tmem + kTmO, tmem + kTmS + (j & 1) * kMlaTile + h * 16 + kk * 8,
-                             umma_desc_sw128(kv + st * Sh::kBlk + kk * 2048, kMlaStages * Sh::kBlk, 1024), kIdPV,
-                             (u > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(tmem + kTmO, umma_desc_sw64(pt + x * Sh::kPBuf + kk * 32, 512),
+                      umma_desc_sw128(kv + st * Sh::kBlk + kk * 2048, kMlaStages * Sh::kBlk, 1024), kIdPV,
+                      (u > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&pv_done[u % 4]);
           umma_commit(&kv_empty[st]);
         }
-        __syncwarp();
-      }
-      if (ok && j + 2 < n_tiles) {  // QK_{j+2} overwrites S[j & 1] after P V of tile j (in issue order)
-        if (!wait_tile(j + 2)) {
-          ok = false;
-          break;
-        }
-        qk(j + 2);
         __syncwarp();
       }
     }
@@ -396,147 +418,112 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       __syncwarp();
       mbar_wait(drain, 0, &g_status_mla);
     }
-  } else if (warp == 6) {
-    // ------------------------------------------------------------ exchange warp
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ score exchange
     const uint32_t peer_rx = dsmem_map(smem_u32(sRx), peer);
     const uint32_t peer_rx_full = dsmem_map(smem_u32(rx_full), peer);
     const uint32_t peer_tx_ok = dsmem_map(smem_u32(tx_ok), peer);
+    int armed0 = 0, armed1 = n_units > 1 ? 1 : -1;
     for (int t = 0; t <= n_units; ++t) {
-      if (t < n_units) {  // staged unit t -> the peer's receive buffer t & 1
-        const int b = t & 1;
-        if (!wait_all(&staged[b], (t >> 1) & 1)) break;
+      if (t < n_units) {  // staged unit t -> the peer's receive slot t % kMlaNX
+        const int x = t % kMlaNX;
+        if (!wait_all(&staged[x], (t / kMlaNX) & 1)) break;
         if (lane == 0)
-          bulk_copy_to_peer(peer_rx + b * Sh::kRxBuf, smem_u32(sStg) + b * Sh::kRxBuf, Sh::kRxBuf, peer_rx_full + b * 8);
+          bulk_copy_to_peer(peer_rx + x * Sh::kXBuf, smem_u32(sStg) + x * Sh::kXBuf, Sh::kXBuf, peer_rx_full + x * 8);
         __syncwarp();
       }
-      const int u = t - 1;  // credit: this CTA has read unit u, so the peer may send unit u + 2
-      if (u >= 0 && u + 2 < n_units) {
-        const int b = u & 1;
-        if (!wait_all(&rx_read[b], (u >> 1) & 1)) break;
-        // Relaxed: the only thing the credit must order is the softmax threads' reads
-        // of the receive buffer, and those have returned before their rx_read arrival
-        // (release), so the peer's next copy cannot overtake them.  A cluster-scope
-        // release here would also wait for the bulk copy issued just before.
-        if (lane == 0) mbar_arrive_remote_relaxed(peer_tx_ok + b * 8);
+      const int u = t - 1;  // credit: this CTA has read unit u, so the peer may send unit u + kMlaNX
+      if (u >= 0 && u + kMlaNX < n_units) {
+        const int x = u % kMlaNX;
+        if (!wait_all(&rx_read[x], (u / kMlaNX) & 1)) break;
+        // Relaxed: the credit orders nothing but the row warps' reads of the receive
+        // slot, which returned before their rx_read arrival (release).
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&rx_full[x], Sh::kXBuf);
+          mbar_arrive_remote_relaxed(peer_tx_ok + x * 8);
+        }
+        if (x) armed1 = u + kMlaNX;
+        else armed0 = u + kMlaNX;
         __syncwarp();
       }
     }
-  } else {
-    // ------------------------------------------------------------ softmax warps
-    const int row = warp * 32 + lane;
-    const int head = h0 + row;
-    const bool row_valid = row < p.hrows && head < p.H;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    {
-      // Q_r of this head: latent dims 256 r .. 256 r + 255 into TMEM columns kTmQ..
-      // as bf16 pairs (the raw row words); rope dims 512 + 32 r .. + 31 into row
-      // `row` of the 64-byte-swizzled shared tile (16-byte chunk c at c ^ ((row >> 1) & 3)).
-      const uint4* src = p.q + ((size_t)s * p.H + (row_valid ? head : 0)) * (kMlaDq / 8);
-      uint32_t qa[64];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint4 v = row_valid ? __ldg(src + 32 * rank + i) : make_uint4(0u, 0u, 0u, 0u);
-        qa[4 * i] = v.x, qa[4 * i + 1] = v.y, qa[4 * i + 2] = v.z, qa[4 * i + 3] = v.w;
-      }
-      uint32_t qb[64];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint4 v = row_valid ? __ldg(src + 32 * rank + 16 + i) : make_uint4(0u, 0u, 0u, 0u);
-        qb[4 * i] = v.x, qb[4 * i + 1] = v.y, qb[4 * i + 2] = v.z, qb[4 * i + 3] = v.w;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 v = row_valid ? __ldg(src + kMlaDv / 8 + 4 * rank + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sQr + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = v;
-      }
-      tmem_st32(lane_base + kTmQ, qa);
-      tmem_st32(lane_base + kTmQ + 32, qa + 32);
-      tmem_st32(lane_base + kTmQ + 64, qb);
-      tmem_st32(lane_base + kTmQ + 96, qb + 32);
-      fence_proxy_async_smem();  // the score UMMA reads the rope tile through the async proxy
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(q_full);
+    // after an abort, let the peer's copies already on their way land before this CTA exits
+    if (lane == 0 && *abort_flag) {
+      if (armed0 >= 0) mbar_wait(&rx_full[0], (armed0 / kMlaNX) & 1, &g_status_mla);
+      if (armed1 >= 0) mbar_wait(&rx_full[1], (armed1 / kMlaNX) & 1, &g_status_mla);
     }
-    const float sl2 = p.scale_log2;
-    const float sgn = sl2 < 0.f ? -1.f : 1.f;
-    const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
-    // staging / receive rows of this head: 8 chunks of 4 floats, chunk c stored at
-    // c ^ (row & 7) so that the 8 rows a quarter-warp touches hit distinct banks
-    const int rsw = row & 7;
-    float* my_stg = sStg + row * kMlaUnit;
-    const float* my_rx = sRx + row * kMlaUnit;
-    auto load_s = [&](int u, uint32_t* v) -> bool {  // this CTA's partial scores of unit u
-      const int j = u >> 1;
-      if ((u & 1) == 0) {
-        if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) return false;
-        tc_fence_after_sync();
-      }
-      tmem_ld32(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * kMlaUnit, v);
-      tmem_ld_wait();
-      return true;
-    };
-    auto stage = [&](int u, const uint32_t* v) -> bool {  // into staging buffer u & 1 for the exchange warp
-      const int b = u & 1;
-      // the copy of unit u - 2 out of this buffer has landed (the peer has even read it)
-      if (u >= 2 && !wait_all(&tx_ok[b], ((u >> 1) - 1) & 1)) return false;
-      float* dst = my_stg + b * (Sh::kRxBuf / 4);
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ P exchange
+    const uint32_t peer_p = dsmem_map(smem_u32(sP), peer);
+    const uint32_t peer_alpha = dsmem_map(smem_u32(sAlpha), peer);
+    const uint32_t peer_p_remote = dsmem_map(smem_u32(p_remote), peer);
+    const uint32_t peer_pslot_ok = dsmem_map(smem_u32(pslot_ok), peer);
+    const uint32_t own_a = (uint32_t)(rank * kMlaOwn * 4);
+    int armed[kMlaNP];
 #pragma unroll
-      for (int c = 0; c < kMlaUnit / 4; ++c)
-        *reinterpret_cast<uint4*>(dst + ((c ^ rsw) << 2)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      fence_proxy_async_smem();  // the bulk copy reads through the async proxy
-      mbar_arrive(&staged[b]);
-      return true;
-    };
-    uint32_t cur[kMlaUnit], nxt[kMlaUnit];
-    int armed0 = 0, armed1 = n_units > 1 ? 1 : -1;  // newest unit each receive buffer is armed for (thread 0)
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = load_s(0, cur) && stage(0, cur);
-    for (int u = 0; ok && u < n_units; ++u) {
-      if (u + 1 < n_units && !(load_s(u + 1, nxt) && stage(u + 1, nxt))) {
+    for (int x = 0; x < kMlaNP; ++x) armed[x] = x < n_units ? x : -1;
+    bool ok = true;
+    for (int t = 0; ok && t <= n_units; ++t) {
+      if (t < n_units) {  // P rows + factors of own heads for unit t -> the peer's P slot t % kMlaNP
+        const int x = t % kMlaNP;
+        if (!wait_all(&p_local[x], (t / kMlaNP) & 1) ||
+            (t >= kMlaNP && !wait_all(&pslot_ok[x], ((t / kMlaNP) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (lane < 4) {  // own heads occupy lanes 32 q + 16 r .. + 15 of each quarter q: 16 rows x 64 B
+          const uint32_t off = x * Sh::kPBuf + (uint32_t)(32 * lane + 16 * rank) * 64;
+          bulk_copy_to_peer(peer_p + off, smem_u32(sP) + off, 16 * 64, peer_p_remote + x * 8);
+        } else if (lane == 4) {
+          bulk_copy_to_peer(peer_alpha + x * kMlaRows * 4 + own_a, smem_u32(sAlpha) + x * kMlaRows * 4 + own_a,
+                            kMlaOwn * 4, peer_p_remote + x * 8);
+        }
+        __syncwarp();
+      }
+      const int u = t - 1;  // credit: P V of unit u completed, so the peer may send unit u + kMlaNP
+      if (u >= 0 && u + kMlaNP < n_units) {
+        const int x = u % kMlaNP;
+        if (!wait_all(&pv_done[u % 4], (u / 4) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&p_remote[x], kPHalfBytes);
+          mbar_arrive_remote_relaxed(peer_pslot_ok + x * 8);
+        }
+#pragma unroll
+        for (int y = 0; y < kMlaNP; ++y)
+          if (y == x) armed[y] = u + kMlaNP;
+        __syncwarp();
+      }
+    }
+    // final row statistics of own heads -> the peer
+    if (ok && wait_all(stat_local, 0) && lane == 0)
+      bulk_copy_to_peer(dsmem_map(smem_u32(sStat), peer) + rank * kMlaOwn * 8, smem_u32(sStat) + rank * kMlaOwn * 8,
+                        kMlaOwn * 8, dsmem_map(smem_u32(stat_full), peer));
+    __syncwarp();
+    if (lane == 0 && *abort_flag) {
+#pragma unroll
+      for (int x = 0; x < kMlaNP; ++x)
+        if (armed[x] >= 0) mbar_wait(&p_remote[x], (armed[x] / kMlaNP) & 1, &g_status_mla);
+      mbar_wait(stat_full, 0, &g_status_mla);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ rescale warps
+    const int quarter = warp - 4;
+    const int hh = 64 * (lane >> 4) + 16 * quarter + (lane & 15);  // head (in the tile) of this lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    bool ok = true;
+    for (int t = 0; ok && t < n_units; ++t) {
+      const int x = t % kMlaNP;
+      if (!wait_all(&p_local[x], (t / kMlaNP) & 1) || !wait_all(&p_remote[x], (t / kMlaNP) & 1)) {
         ok = false;
         break;
       }
-      const int b = u & 1, j = u >> 1;
-      if (!wait_all(&rx_full[b], (u >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      float sc[kMlaUnit];
-      const float* rx = my_rx + b * (Sh::kRxBuf / 4);
-#pragma unroll
-      for (int c = 0; c < kMlaUnit / 4; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(rx + ((c ^ rsw) << 2));
-        sc[4 * c] = __uint_as_float(cur[4 * c]) + v.x;
-        sc[4 * c + 1] = __uint_as_float(cur[4 * c + 1]) + v.y;
-        sc[4 * c + 2] = __uint_as_float(cur[4 * c + 2]) + v.z;
-        sc[4 * c + 3] = __uint_as_float(cur[4 * c + 3]) + v.w;
-      }
-      mbar_arrive(&rx_read[b]);
-      // re-arm buffer b for unit u + 2: its data cannot arrive before every thread here
-      // has read unit u (the peer waits for the credit that rx_read leads to)
-      if (threadIdx.x == 0 && u + 2 < n_units) {
-        mbar_arrive_expect_tx(&rx_full[b], Sh::kRxBuf);
-        if (b) armed1 = u + 2;
-        else armed0 = u + 2;
-      }
-      const int vis = min(kMlaUnit, t1 - (t0 + u * kMlaUnit));
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kMlaUnit; ++c) mx[c & 7] = fmaxf(mx[c & 7], c < vis ? sc[c] * sgn : -INFINITY);
-      const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
-      const bool grow = m_new > m_run + 8.0f;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = exp2_approx(m_run - m_new);
-        m_run = m_new;
-      }
-      if (u >= 1 && __any_sync(0xffffffffu, grow)) {
-        // O_r holds every earlier unit only once P V of unit u - 1 completed
-        if (!wait_all(&pv_done[(u - 1) % 4], ((u - 1) / 4) & 1)) {
+      const float a = sAlpha[x * kMlaRows + hh];
+      if (t >= 1 && __any_sync(0xffffffffu, a != 1.0f)) {
+        // O holds every earlier unit only once P V of unit t - 1 completed
+        if (!wait_all(&pv_done[(t - 1) % 4], ((t - 1) / 4) & 1)) {
           ok = false;
           break;
         }
@@ -547,81 +534,223 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           tmem_ld32(lane_base + kTmO + c * 32, ov);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
           tmem_st32(lane_base + kTmO + c * 32, ov);
         }
+        tmem_st_wait();
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&p_relay[x]);
+    }
+  } else {
+    // ------------------------------------------------------------ row warps
+    const int quarter = warp;
+    const int g = lane >> 4, li = lane & 15;
+    const bool own = g == (int)rank;
+    const int xi = 16 * quarter + li;               // row within a 64-head half
+    const int hh = 64 * g + xi;                      // head (in the tile) of this lane
+    const int head = h0 + hh;
+    const bool row_valid = hh < p.hrows && head < p.H;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int prow = 32 * quarter + 16 * (int)rank + li;  // P row / TMEM lane of the own head this lane works on
+    const int tok_half = own ? 0 : 16;                // tokens of a unit this lane exponentiates
+    {
+      // Q_r of this lane's head: latent dims 256 r .. 256 r + 255 into TMEM columns
+      // kTmQ.. as bf16 pairs (the raw row words), rope dims 512 + 32 r .. + 31 into
+      // row `lane` of the 64-byte-swizzled shared tile (chunk c at c ^ ((row >> 1) & 3)).
+      const uint4* src = p.q + ((size_t)s * p.H + (row_valid ? head : 0)) * (kMlaDq / 8);
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x4 = row_valid ? __ldg(src + 32 * rank + c0 / 4 + i) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * i] = x4.x, v[4 * i + 1] = x4.y, v[4 * i + 2] = x4.z, v[4 * i + 3] = x4.w;
+        }
+        tmem_st32(lane_base + kTmQ + c0, v);
+      }
+      const int row = 32 * quarter + lane;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 x4 = row_valid ? __ldg(src + kMlaDv / 8 + 4 * rank + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sQr + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = x4;
+      }
+      fence_proxy_async_smem();  // the score UMMA reads the rope tile through the async proxy
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(q_full);
+    }
+    const float sl2 = p.scale_log2;
+    const float sgn = sl2 < 0.f ? -1.f : 1.f;
+    const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
+    auto load_s = [&](int u, uint32_t* v) -> bool {  // this CTA's partial scores of unit u, every lane
+      const int j = u >> 1;
+      if ((u & 1) == 0) {
+        if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) return false;
+        tc_fence_after_sync();
+      }
+      tmem_ld32(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * kMlaUnit, v);
+      tmem_ld_wait();
+      if ((u & 1) == 1 || u + 1 == n_units) {  // last read of S[j & 1] for tile j
+        tc_fence_before_sync();
+        mbar_arrive(&s_free[j & 1]);
+      }
+      return true;
+    };
+    auto stage = [&](int u, const uint32_t* v) -> bool {  // the peer's heads of unit u -> staging slot
+      const int x = u % kMlaNX;
+      if (u >= kMlaNX && !wait_all(&tx_ok[x], ((u / kMlaNX) - 1) & 1)) return false;
+      if (!own) {
+        uint8_t* dst = sStg + x * Sh::kXBuf + xi * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(dst + ((c ^ (xi & 7)) << 4)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();  // the bulk copy reads through the async proxy
+      }
+      mbar_arrive(&staged[x]);
+      return true;
+    };
+    uint32_t cur[kMlaUnit], nxt[kMlaUnit];
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = load_s(0, cur) && stage(0, cur);
+    for (int u = 0; ok && u < n_units; ++u) {
+      if (u + 1 < n_units && !(load_s(u + 1, nxt) && stage(u + 1, nxt))) {
+        ok = false;
+        break;
+      }
+      const int x = u % kMlaNX;
+      if (!wait_all(&rx_full[x], (u / kMlaNX) & 1)) {
+        ok = false;
+        break;
+      }
+      float sc[kMlaUnit];
+      if (own) {
+        const uint8_t* rx = sRx + x * Sh::kXBuf + xi * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 r4 = *reinterpret_cast<const float4*>(rx + ((c ^ (xi & 7)) << 4));
+          sc[4 * c] = __uint_as_float(cur[4 * c]) + r4.x;
+          sc[4 * c + 1] = __uint_as_float(cur[4 * c + 1]) + r4.y;
+          sc[4 * c + 2] = __uint_as_float(cur[4 * c + 2]) + r4.z;
+          sc[4 * c + 3] = __uint_as_float(cur[4 * c + 3]) + r4.w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kMlaUnit; ++c) sc[c] = 0.f;
+      }
+      mbar_arrive(&rx_read[x]);
+      // lane pair (i, i ^ 16) splits the own head's unit: the own lane keeps tokens 0..15,
+      // the partner takes tokens 16..31
+      float mine[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float hi = __shfl_xor_sync(0xffffffffu, sc[16 + k], 16);
+        mine[k] = own ? sc[k] : hi;
+      }
+      const int vis = min(kMlaUnit, t1 - (t0 + u * kMlaUnit)) - tok_half;  // visible tokens among mine
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 16; ++c) mx[c & 3] = fmaxf(mx[c & 3], c < vis ? mine[c] * sgn : -INFINITY);
+      float mxa = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 16));
+      const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
+      float alpha = 1.f;
+      if (m_new > m_run + 8.0f) {
+        alpha = exp2_approx(m_run - m_new);
+        m_run = m_new;
       }
       l_run *= alpha;
       const float neg_m = -m_run;
-      float ls[8];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-      uint32_t pk[kMlaUnit / 2];
-#pragma unroll
-      for (int c = 0; c < kMlaUnit; c += 2) {
-        const float e0 = c < vis ? exp2_approx(fmaf(sc[c] * sgn, asl2, neg_m)) : 0.f;
-        const float e1 = c + 1 < vis ? exp2_approx(fmaf(sc[c + 1] * sgn, asl2, neg_m)) : 0.f;
-        ls[c & 7] += e0;
-        ls[(c + 1) & 7] += e1;
+      for (int c = 0; c < 16; c += 2) {
+        const float e0 = c < vis ? exp2_approx(fmaf(mine[c] * sgn, asl2, neg_m)) : 0.f;
+        const float e1 = c + 1 < vis ? exp2_approx(fmaf(mine[c + 1] * sgn, asl2, neg_m)) : 0.f;
+        ls[c & 3] += e0;
+        ls[(c + 1) & 3] += e1;
         pk[c >> 1] = pack_bf16x2(e0, e1);
       }
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tmem_st16(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * 16, pk);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&p_full[u % 4]);
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // P slot u % kMlaNP is free once P V of unit u - kMlaNP completed
+      const int xp = u % kMlaNP;
+      if (u >= kMlaNP && !wait_all(&pv_done[(u - kMlaNP) % 4], ((u - kMlaNP) / 4) & 1)) {
+        ok = false;
+        break;
+      }
+      uint8_t* pr = sP + xp * Sh::kPBuf + prow * 64;
+      const int sw = (prow >> 1) & 3, c0 = own ? 0 : 2;
+      *reinterpret_cast<uint4*>(pr + ((c0 ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(pr + (((c0 + 1) ^ sw) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      if (own) sAlpha[xp * kMlaRows + hh] = alpha;
+      fence_proxy_async_smem();  // P V and the bulk copy read P through the async proxy
+      mbar_arrive(&p_local[xp]);
 #pragma unroll
       for (int c = 0; c < kMlaUnit; ++c) cur[c] = nxt[c];
     }
     if (ok && wait_all(&pv_done[(n_units - 1) % 4], ((n_units - 1) / 4) & 1)) {
-      tc_fence_after_sync();
-      const float inv = 1.0f / l_run;
-      const size_t sh = (size_t)s * p.H + head;
+      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // the own head's row sum
+      if (own) {
+        sStat[hh * 2] = m_run;
+        sStat[hh * 2 + 1] = l_tot;
+        fence_proxy_async_smem();  // copied to the peer by the bulk engine
+      }
+      mbar_arrive(stat_local);
+      // this lane's row: an own head (local statistics) or a peer head (the peer's)
+      bool have = true;
+      float inv = 0.f;
+      if (own) {
+        inv = 1.0f / l_tot;
+      } else {
+        have = false;
+      }
+      if (!__all_sync(0xffffffffu, have)) {
+        if (!wait_all(stat_full, 0)) ok = false;
+        if (!own) inv = 1.0f / sStat[hh * 2 + 1];
+      }
+      if (ok) {
+        tc_fence_after_sync();
+        const size_t sh = (size_t)s * p.H + head;
 #pragma unroll 1
-      for (int c = 0; c < kMlaHalf / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(lane_base + kTmO + c * 32, ov);
-        tmem_ld_wait();
-        if (!row_valid) continue;
-        if (direct) {
-          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf + c * 32;
+        for (int c = 0; c < kMlaHalf / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + kTmO + c * 32, ov);
+          tmem_ld_wait();
+          if (!row_valid) continue;
+          if (direct) {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf + c * 32;
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
-            *reinterpret_cast<uint4*>(o + i) = v;
+            for (int i = 0; i < 32; i += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+              *reinterpret_cast<uint4*>(o + i) = v;
+            }
+          } else {
+            float* o = p.part_out + (sh * p.max_parts + part) * kMlaDv + rank * kMlaHalf + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(o + i) =
+                  make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                              __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
           }
-        } else {
-          float* o = p.part_out + (sh * p.max_parts + part) * kMlaDv + rank * kMlaHalf + c * 32;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(o + i) =
-                make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                            __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+        }
+        if (row_valid && own) {
+          const float lse = (m_run + log2f(l_tot)) * kLn2;
+          if (direct) {
+            if (p.lse_out) p.lse_out[sh] = lse;
+          } else {
+            p.part_lse[sh * p.max_parts + part] = lse;
+          }
         }
       }
-      if (row_valid && rank == 0) {
-        const float lse = (m_run + log2f(l_run)) * kLn2;
-        if (direct) {
-          if (p.lse_out) p.lse_out[sh] = lse;
-        } else {
-          p.part_lse[sh * p.max_parts + part] = lse;
-        }
-      }
-    }
-    // after an abort, let the peer's copies already on their way land before this CTA exits
-    if (threadIdx.x == 0 && *abort_flag) {
-      if (armed0 >= 0) mbar_wait(&rx_full[0], (armed0 >> 1) & 1, &g_status_mla);
-      if (armed1 >= 0) mbar_wait(&rx_full[1], (armed1 >> 1) & 1, &g_status_mla);
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kMlaTmemCols);
   }
