@@ -436,7 +436,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         tmem_ld_wait();
         if (lean) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
+          for (int c = 0; c < 64; c += 2)
+            mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
         } else {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -467,9 +468,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       // pass 2: P = exp2(s * |sl2| - m) as bf16 pairs (even token in the low half), 64 tokens
       // at a time, over the first 64 columns of S_w (columns already consumed)
       const float neg_m = -m_run;
-      float ls[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // row sums, as packed pairs
+      const uint64_t asl2_2 = f2_pack(asl2, asl2), neg_m2 = f2_pack(neg_m, neg_m);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[64];
@@ -478,12 +478,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         tmem_ld_wait();
         uint32_t pk[32];
         if (lean) {
+          // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float e0 = exp2_approx(fmaf(__uint_as_float(sv[c]), asl2, neg_m));
-            const float e1 = exp2_approx(fmaf(__uint_as_float(sv[c + 1]), asl2, neg_m));
-            ls[c & 7] += e0;
-            ls[(c + 1) & 7] += e1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
+            const float e0 = exp2_approx(x0);
+            const float e1 = exp2_approx(x1);
+            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
             pk[c >> 1] = pack_bf16x2(e0, e1);
           }
         } else {
@@ -492,13 +494,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
             const int t = half * 64 + c;
             const float e0 = t < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
             const float e1 = t + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
-            ls[c & 7] += e0;
-            ls[(c + 1) & 7] += e1;
+            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
             pk[c >> 1] = pack_bf16x2(e0, e1);
           }
         }
         tmem_st32(s_tmem + half * 32, pk);
       }
+      float ls[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f2_unpack(ls2[i], ls[2 * i], ls[2 * i + 1]);
       l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_st_wait();
       tc_fence_before_sync();
