@@ -40,6 +40,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch.  pdl_launch_dependents(): the next kernel in
+// the stream may start launching once every CTA of this grid has executed it
+// (or exited).  pdl_wait(): block until the previous grid in the stream has
+// completed and its memory is visible (a no-op without such a dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

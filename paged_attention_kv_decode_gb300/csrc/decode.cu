@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   constexpr int STAGE_BYTES = Shape::kStageBytes;
   constexpr int KS = Shape::kSteps;
   static_assert(NW * (64 + D * 32) <= NW * STAGES * STAGE_BYTES, "combine area must fit in the ring");
+  pdl_launch_dependents();  // the merge may start launching; it waits for this grid to finish
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
@@ -372,6 +373,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
                                                                      const float* __restrict__ v_cache,
                                                                      const DecodeParams p) {
   constexpr int DPL = D / 32;  // dims per lane
+  pdl_launch_dependents();
   __shared__ float cm[kF32Warps * 8], cl[kF32Warps * 8];
   __shared__ float co[kF32Warps * D * 8];
 
@@ -458,6 +460,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   constexpr int NWARP = kMergeThreads / 32;
   __shared__ float red[NWARP];
   __shared__ float4 acc_s[NWARP][kMergeMaxD / 4];
+  pdl_wait();  // the partials of the kernel before this one are complete and visible
   const size_t sh = blockIdx.x;
   const int s = (int)(sh / H);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -547,6 +550,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* 
                                                                    float* __restrict__ lse_out, int S, int H, int D,
                                                                    int max_parts, int skip_single) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();  // the partials of the kernel before this one are complete and visible
   const size_t sh = (size_t)blockIdx.x * (kMergeThreads / 32) + warp;
   if (sh >= (size_t)S * H) return;
   const int s = (int)(sh / H);
@@ -621,28 +625,25 @@ int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t*
                     float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int skip_single,
                     cudaStream_t st) {
   const size_t pairs = (size_t)S * H;
+  // launched as a programmatic dependent: its launch overlaps the tail of the kernel
+  // that wrote the partials, and it waits (pdl_wait) for that kernel to finish
   if (max_parts <= 16) {
-    const unsigned grid = (unsigned)((pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
+    const dim3 grid((unsigned)((pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32)));
     if (out_dtype == METIS_BF16)
-      merge_warp_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(
-          part_out, part_lse, seq_lens, P, reinterpret_cast<__nv_bfloat16*>(out), lse_out, S, H, D, max_parts,
-          skip_single);
-    else
-      merge_warp_kernel<float><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
-                                                                reinterpret_cast<float*>(out), lse_out, S, H, D,
-                                                                max_parts, skip_single);
-  } else {
-    const unsigned grid = (unsigned)pairs;
-    if (out_dtype == METIS_BF16)
-      merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
-                                                                   reinterpret_cast<__nv_bfloat16*>(out), lse_out, H,
-                                                                   D, max_parts, skip_single);
-    else
-      merge_kernel<float><<<grid, kMergeThreads, 0, st>>>(part_out, part_lse, seq_lens, P,
-                                                           reinterpret_cast<float*>(out), lse_out, H, D, max_parts,
-                                                           skip_single);
+      return launch_dependent(merge_warp_kernel<__nv_bfloat16>, grid, dim3(kMergeThreads), 0, st, "merge kernel launch",
+                              part_out, part_lse, seq_lens, P, reinterpret_cast<__nv_bfloat16*>(out), lse_out, S, H, D,
+                              max_parts, skip_single);
+    return launch_dependent(merge_warp_kernel<float>, grid, dim3(kMergeThreads), 0, st, "merge kernel launch", part_out,
+                            part_lse, seq_lens, P, reinterpret_cast<float*>(out), lse_out, S, H, D, max_parts,
+                            skip_single);
   }
-  return check_launch("merge kernel launch");
+  const dim3 grid((unsigned)pairs);
+  if (out_dtype == METIS_BF16)
+    return launch_dependent(merge_kernel<__nv_bfloat16>, grid, dim3(kMergeThreads), 0, st, "merge kernel launch",
+                            part_out, part_lse, seq_lens, P, reinterpret_cast<__nv_bfloat16*>(out), lse_out, H, D,
+                            max_parts, skip_single);
+  return launch_dependent(merge_kernel<float>, grid, dim3(kMergeThreads), 0, st, "merge kernel launch", part_out,
+                          part_lse, seq_lens, P, reinterpret_cast<float*>(out), lse_out, H, D, max_parts, skip_single);
 }
 
 static int launch_merge(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,

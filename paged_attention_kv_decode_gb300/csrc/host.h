@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/metis_attn.h"
+
 namespace metis {
 
 // Record a message for metis_last_error() and return `code`.
@@ -21,6 +23,28 @@ int check_launch(const char* what);
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  CUtensorMapSwizzle swizzle);
+
+// Launch `kernel` as a programmatic dependent of the previous kernel in the
+// stream: it may start launching while that kernel still runs, so it must
+// execute pdl_wait() (common.cuh) before touching anything the previous kernel
+// writes.  Returns METIS_OK or METIS_E_CUDA.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const char* what,
+                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return fail(METIS_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return METIS_OK;
+}
 
 // Raise a kernel's dynamic shared memory limit once per device.
 int set_max_dynamic_smem(const void* func, int bytes, int* done_mask);

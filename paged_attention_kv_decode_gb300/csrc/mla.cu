@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, i
                                                             int max_items) {
   __shared__ int scan[1024];
   __shared__ int4 buf[kMlaSortMax];
+  pdl_launch_dependents();  // the attention kernel may start launching (it waits for the items)
   const int tid = threadIdx.x;
   const int per = (p.S + 1023) / 1024;
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
@@ -176,6 +177,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKVh,
                       const MlaParams p) {
   using Sh = MlaShape;
+  pdl_wait();               // the schedule kernel's items are complete and visible
+  pdl_launch_dependents();  // the merge may start launching; it waits for this grid to finish
   extern __shared__ uint8_t smem_raw[];
   const uint32_t slack = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + slack;
@@ -877,8 +880,8 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   static int done = 0;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), MlaShape::kSmem, &done);
   if (rc) return rc;
-  mla_decode_kernel<<<(unsigned)(lay.max_items * head_tiles * 2), kMlaThreads, MlaShape::kSmem, st>>>(tmKV, tmKVh, p);
-  rc = check_launch("mla_decode_kernel launch");
+  rc = launch_dependent(mla_decode_kernel, dim3((unsigned)(lay.max_items * head_tiles * 2)), dim3(kMlaThreads),
+                        MlaShape::kSmem, st, "mla_decode_kernel launch", tmKV, tmKVh, p);
   if (rc) return rc;
   if (partition_size > 0 && lay.max_parts > 1)
     rc = launch_merge_ex(p.part_out, p.part_lse, seq_lens, partition_size, out, lse_out, num_seqs, num_heads, kMlaDv,

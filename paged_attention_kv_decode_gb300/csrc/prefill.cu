@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
                                                                           int* count, int max_items) {
   __shared__ int scan[kSchedThreads];
   __shared__ int4 buf[kSortMax];
+  pdl_launch_dependents();  // the attention kernel may start launching (it waits for the items)
   const int tid = threadIdx.x;
   const int per = (p.S + kSchedThreads - 1) / kSchedThreads;
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
                                                                        const PrefillParams p) {
   using Sh = PfShape<D>;
   constexpr int HALVES = Sh::kHalves;
+  pdl_wait();  // the schedule kernel's items are complete and visible
   extern __shared__ uint8_t smem_raw[];
   const uint32_t slack = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + slack;
@@ -592,8 +594,8 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
   auto kern = prefill_bf16_kernel<D>;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem, &done);
   if (rc) return rc;
-  kern<<<(unsigned)(max_items * p.G), kPfThreads, smem, st>>>(tmQ, tmK, tmV, p);
-  return check_launch("prefill_bf16_kernel launch");
+  return launch_dependent(kern, dim3((unsigned)(max_items * p.G)), dim3(kPfThreads), smem, st,
+                          "prefill_bf16_kernel launch", tmQ, tmK, tmV, p);
 }
 
 }  // namespace metis
