@@ -51,6 +51,7 @@ WORKLOAD = ("batched paged decode, bf16 KV: 64 seqs, seq_lens U[512,4096], 32 q 
             "block_size 16, block_table a random permutation of the pool")
 PARTITION = 1024
 MLA_PARTITION = 2048
+NOMINAL_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth; fractions are reported against it and the measured peak
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TC_TFLOPS = (1900.0, 1700.0)
 
@@ -395,6 +396,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": world * S * args.steps / (total_ms * 1e-3),
         "hbm_frac": value / peak,
+        "hbm_frac_nominal": value / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel", "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": achieved / peak,
@@ -466,6 +468,7 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
                                                                   stream=stream), reps, flush, stream)
         nb = decode_algorithmic_bytes(c)
         res["long_split_decode"] = {"ms": med, "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm,
+                                    "hbm_frac_nominal": nb / med / 1e6 / NOMINAL_HBM_GBS,
                                     "kv_bytes": nb, "partition_size": c.partition_size,
                                     "tokens_per_s": c.S / (med * 1e-3)}
         del t, out, ws, c
@@ -505,7 +508,9 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         nb = tok * 576 * 2 + c.S * c.H * (576 + 512) * 2 + int(sum(-(-int(L) // c.bs) for L in c.seq_lens)) * 4
         tf = flops / med / 1e9
         res["mla_decode"] = {"ms": med, "TFLOP_s": tf, "tensor_frac_burst": tf / tc_burst,
-                             "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm, "flops": flops,
+                             "tensor_frac_sustained": tf / tc_sus,
+                             "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm,
+                             "hbm_frac_nominal": nb / med / 1e6 / NOMINAL_HBM_GBS, "flops": flops,
                              "bytes": nb, "tokens": tok, "partition_size": P,
                              "tokens_per_s": c.S / (med * 1e-3)}
         del t, out, ws, c

@@ -19,3 +19,4 @@ from .attention import (  # noqa: F401
     softmax_attention,
     split_partials,
 )
+from .cache_write import mla_reshape_and_cache, reshape_and_cache  # noqa: F401,E402
