@@ -14,8 +14,9 @@ timed events.
 
 The line also carries ``workloads``: the tiny fp32 decode, the long-context
 split-KV decode (GB/s), the chunked prefill mixed with decodes (TFLOP/s against
-the measured bf16 peak) and the MLA decode (TFLOP/s and GB/s), each timed the
-same way as one call of its entry point.
+the measured bf16 peak), the MLA decode (TFLOP/s and GB/s) and the paged KV
+write of the chunked-prefill step's new rows (GB/s), each timed the same way as
+one call of its entry point.
 
 ``value`` is decode KV GB/s: the algorithmic bytes of a step (every cached
 token's K and V row for its KV head, the queries, outputs, block-table
@@ -494,6 +495,30 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
                                   "note": "one call: 16 chunks of 512 over cached prefixes + 48 single-token decodes"}
         del t, out, ws, c
         torch.cuda.empty_cache()
+    if "kvw" in names:
+        # the paged KV write in front of the chunked-prefill step: its 8240 new K/V rows
+        c = wl.config4_chunked_prefill()
+        cu = c.cu_q_lens.numpy()
+        lens = c.seq_lens.numpy().astype(np.int64)
+        bt = c.block_table.numpy()
+        slots = []
+        for si in range(c.S):
+            ql = int(cu[si + 1] - cu[si])
+            tt = np.arange(lens[si] - ql, lens[si])
+            slots.append(bt[si, tt // c.bs].astype(np.int64) * c.bs + tt % c.bs)
+        slots = torch.from_numpy(np.concatenate(slots)).to(dev)
+        g = torch.Generator().manual_seed(12)
+        key = torch.randn(c.T, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
+        value = torch.randn(c.T, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
+        kc, vc = c.k_cache.to(dev), c.v_cache.to(dev)
+        med, mn = _time_calls(lambda: pa.metis_reshape_and_cache(key, value, kc, vc, slots, stream=stream), reps, flush,
+                              stream)
+        nb = 2 * 2 * c.T * c.G * c.D * 2 + c.T * 8    # K and V rows read and written, plus the slots
+        res["kv_write"] = {"ms": med, "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm,
+                           "hbm_frac_nominal": nb / med / 1e6 / NOMINAL_HBM_GBS, "bytes": nb, "tokens": c.T,
+                           "note": "the chunked-prefill step's new K/V rows scattered into their pages"}
+        del key, value, kc, vc, slots, c
+        torch.cuda.empty_cache()
     if "c5" in names:
         c = wl.config5_mla_decode()
         t = [x.to(dev) for x in (c.q, c.kv_cache, c.block_table, c.seq_lens)]
@@ -526,8 +551,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=PARTITION)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workloads", default="c1,c3,c4,c5",
-                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5; empty: none)")
+    ap.add_argument("--workloads", default="c1,c3,c4,c5,kvw",
+                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw; empty: none)")
     ap.add_argument("--workload-reps", type=int, default=20)
     ap.add_argument("--ramp-steps", type=int, default=None,
                     help="untimed steps before warm-up (default: about one second of steps)")

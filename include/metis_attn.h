@@ -274,6 +274,47 @@ int metis_merge_attn_states(const float* part_out, const float* part_lse, const 
                             int out_dtype, void* stream);
 
 /*
+ * metis_reshape_and_cache -- write one step's new key/value rows into their
+ * pages, the step in front of every attention call (vLLM's cache manager owns
+ * one paged KV layer per attention layer: vllm-metis 0.1.0 page, "How the
+ * model maps onto vLLM", "Caches"; the scheduler's block table addresses the
+ * same pages: vllm-metal article, section 4).  For n < num_tokens with
+ * slot = slot_mapping[n] >= 0:
+ *   k_cache[slot / block_size, slot % block_size, :, :] = key[n, :, :]
+ *   v_cache[slot / block_size, slot % block_size, :, :] = value[n, :, :]
+ *
+ *   key, value     [num_tokens, num_kv_heads, head_dim], dtype, contiguous
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], dtype
+ *   slot_mapping   int64 [num_tokens]: block id * block_size + offset; < 0 is a
+ *                  padding token (not written)
+ *   dtype          METIS_F32 or METIS_BF16 (a byte copy)
+ * All pointers are caller-owned device memory, 16-byte aligned (slot_mapping
+ * 8-byte); num_kv_heads * head_dim * element size must be a multiple of 16.
+ * Two tokens with the same slot: one of the two rows is written (which one is
+ * unspecified).  A slot >= num_blocks * block_size is not written and sets
+ * METIS_STATUS_BAD_BLOCK_ID.  Returns METIS_OK or METIS_E_* (nothing launched);
+ * num_tokens == 0 is a successful no-op.  Asynchronous on `stream`.
+ */
+int metis_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                            const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, int dtype, void* stream);
+
+/*
+ * metis_mla_reshape_and_cache -- the same write for the MLA latent cache
+ * (vllm-metal article, section 3): row [c_kv | k_pe] of token n goes to
+ *   kv_cache[slot / block_size, slot % block_size, 0 : d_latent] = kv_c[n, :]
+ *   kv_cache[slot / block_size, slot % block_size, d_latent :]   = k_pe[n, :]
+ *
+ *   kv_c   bf16 [num_tokens, d_latent];  k_pe  bf16 [num_tokens, d_rope]
+ *   kv_cache  bf16 [num_blocks, block_size, d_latent + d_rope]
+ *   slot_mapping  int64 [num_tokens], as above
+ * d_latent and d_rope multiples of 8; alignment, errors and status as above.
+ */
+int metis_mla_reshape_and_cache(const void* kv_c, const void* k_pe, void* kv_cache,
+                                const int64_t* slot_mapping, int num_tokens, int d_latent, int d_rope,
+                                int block_size, int num_blocks, void* stream);
+
+/*
  * metis_read_status -- the device status word (METIS_STATUS_* bits, OR-ed
  * over every launch since it was last cleared) of the current device.
  * Synchronises the device: for tests and debugging, not for the hot path.

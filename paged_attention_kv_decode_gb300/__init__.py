@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     metis_last_error,
     metis_merge_attn_states,
     metis_mla_decode,
+    metis_mla_reshape_and_cache,
     metis_mla_workspace_bytes,
     NOALLOC_SCRATCH_BYTES,
     metis_paged_attn_decode,
@@ -31,5 +32,6 @@ from ._binding import (  # noqa: F401
     metis_prefill_workspace_bytes,
     split_workspace_views,
     metis_read_status,
+    metis_reshape_and_cache,
     metis_version,
 )

@@ -72,6 +72,8 @@ SIGNATURES = {
     "metis_read_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
     "metis_last_error": (ctypes.c_char_p, []),
     "metis_version": (_i, []),
+    "metis_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    "metis_mla_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
 }
 
 
@@ -362,3 +364,41 @@ def metis_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch
                                 float(scale), int(partition_size), int(max_seq_len), _ptr(workspace), ws_bytes,
                                 _stream(stream)))
     return out, lse_out
+
+
+def metis_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write ``key`` / ``value`` rows ``[N, G, D]`` into the paged caches ``[nb, bs, G, D]``
+    at ``slot_mapping`` (int64 ``[N]``, negative = padding); in place, asynchronous."""
+    lib = load_library()
+    _cuda("key", key, ndim=3)
+    dt = key.dtype
+    _cuda("value", value, dtype=dt, ndim=3)
+    _cuda("k_cache", k_cache, dtype=dt, ndim=4)
+    _cuda("v_cache", v_cache, dtype=dt, ndim=4)
+    _cuda("slot_mapping", slot_mapping, dtype=torch.int64, ndim=1)
+    N, G, D = key.shape
+    nb, bs = k_cache.shape[:2]
+    if (value.shape != key.shape or tuple(k_cache.shape[2:]) != (G, D) or v_cache.shape != k_cache.shape
+            or slot_mapping.shape[0] != N):
+        raise ValueError("inconsistent shapes")
+    _check(lib.metis_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                       N, G, D, bs, nb, _dtype_code(dt), _stream(stream)))
+
+
+def metis_mla_reshape_and_cache(kv_c: torch.Tensor, k_pe: torch.Tensor, kv_cache: torch.Tensor,
+                                slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write rows ``[kv_c | k_pe]`` (bf16 ``[N, d_latent]``, ``[N, d_rope]``) into the latent
+    cache ``[nb, bs, d_latent + d_rope]`` at ``slot_mapping``; in place, asynchronous."""
+    lib = load_library()
+    _cuda("kv_c", kv_c, dtype=torch.bfloat16, ndim=2)
+    _cuda("k_pe", k_pe, dtype=torch.bfloat16, ndim=2)
+    _cuda("kv_cache", kv_cache, dtype=torch.bfloat16, ndim=3)
+    _cuda("slot_mapping", slot_mapping, dtype=torch.int64, ndim=1)
+    N, dl = kv_c.shape
+    dr = k_pe.shape[1]
+    nb, bs, dk = kv_cache.shape
+    if k_pe.shape[0] != N or dk != dl + dr or slot_mapping.shape[0] != N:
+        raise ValueError("inconsistent shapes")
+    _check(lib.metis_mla_reshape_and_cache(_ptr(kv_c), _ptr(k_pe), _ptr(kv_cache), _ptr(slot_mapping), N, dl, dr,
+                                           bs, nb, _stream(stream)))

@@ -63,5 +63,6 @@ int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t*
 int decode_status(uint32_t* bits, int clear);
 int prefill_status(uint32_t* bits, int clear);
 int mla_status(uint32_t* bits, int clear);
+int cache_status(uint32_t* bits, int clear);
 
 }  // namespace metis

@@ -187,3 +187,35 @@ def test_mla_workspace_bytes(lib):
     assert pa.metis_mla_workspace_bytes(4, 128, 512, 0) > 0
     n = pa.metis_mla_workspace_bytes(4, 128, 512, 256)       # 2 partitions of fp32 partials
     assert n >= 4 * 128 * 2 * 512 * 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), -2), (dict(key=None), -1), (dict(slots=None), -1), (dict(dt=3), -3),
+    (dict(G=1, D=4, dt=pa.METIS_BF16), -3),                 # 8-byte rows cannot be copied as 16-byte vectors
+    (dict(key=FAKE + 8), -4), (dict(slots=FAKE + 4), -4), (dict(G=0), -2), (dict(nb=0), -2),
+])
+def test_reshape_and_cache_rejects(lib, kw, code):
+    a = dict(key=FAKE, value=FAKE, kc=FAKE, vc=FAKE, slots=FAKE, n=16, G=8, D=128, bs=16, nb=64, dt=pa.METIS_BF16)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.metis_reshape_and_cache(vp(a["key"]), vp(a["value"]), vp(a["kc"]), vp(a["vc"]), vp(a["slots"]), a["n"],
+                                     a["G"], a["D"], a["bs"], a["nb"], a["dt"], None)
+    assert rc == code
+
+
+def test_reshape_and_cache_empty_is_a_no_op(lib):
+    vp = ctypes.c_void_p
+    assert lib.metis_reshape_and_cache(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 0, 8, 128, 16, 64,
+                                       pa.METIS_BF16, None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), -2), (dict(kv_c=None), -1), (dict(dl=500), -3), (dict(dr=0), -2), (dict(kv=FAKE + 8), -4),
+])
+def test_mla_reshape_and_cache_rejects(lib, kw, code):
+    a = dict(kv_c=FAKE, k_pe=FAKE, kv=FAKE, slots=FAKE, n=16, dl=512, dr=64, bs=64, nb=32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.metis_mla_reshape_and_cache(vp(a["kv_c"]), vp(a["k_pe"]), vp(a["kv"]), vp(a["slots"]), a["n"], a["dl"],
+                                         a["dr"], a["bs"], a["nb"], None)
+    assert rc == code
