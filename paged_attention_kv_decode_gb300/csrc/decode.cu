@@ -159,6 +159,28 @@ constexpr int bf16_decode_smem_bytes() {
   return 1024 + NW * STAGES * Bf16DecodeShape<D>::kStageBytes + NW * STAGES * 8;
 }
 
+// Longest-first order for the unsplit path: CTAs launch in grid order, so the
+// CTA with z-index k takes the sequence of rank k by length (ties: lower index
+// first).  Every CTA ranks the whole batch itself -- S^2 / blockDim comparisons in
+// shared memory, small for the batches it is used on (kMaxRankSeqs) -- which
+// needs no schedule kernel and no workspace.  The heaviest sequences start first
+// and the short ones fill the SMs that free up, instead of a ragged last wave.
+constexpr int kMaxRankSeqs = 128;
+
+__device__ __forceinline__ int seq_of_rank(const DecodeParams& p, int rank, int* lens, int* found) {
+  for (int i = threadIdx.x; i < p.S; i += blockDim.x) lens[i] = min(max(p.seq_lens[i], 0), p.cap);
+  if (threadIdx.x == 0) *found = rank;
+  __syncthreads();
+  for (int c = threadIdx.x; c < p.S; c += blockDim.x) {
+    const int Lc = lens[c];
+    int r = 0;
+    for (int k = 0; k < p.S; ++k) r += (lens[k] > Lc) || (lens[k] == Lc && k < c);
+    if (r == rank) *found = c;
+  }
+  __syncthreads();
+  return *found;
+}
+
 template <int D, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV,
@@ -174,7 +196,11 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * STAGES * STAGE_BYTES);
 
-  const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  __shared__ int rank_lens[kMaxRankSeqs];
+  __shared__ int rank_found;
+  const int part = blockIdx.x, g = blockIdx.y;
+  const int s = (p.partition_size == 0 && p.S <= kMaxRankSeqs) ? seq_of_rank(p, blockIdx.z, rank_lens, &rank_found)
+                                                                : (int)blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int t0, t1;
   if (!decode_range<__nv_bfloat16>(p, part, g, s, t0, t1)) return;

@@ -19,8 +19,10 @@ from helpers import assert_lse, assert_parity, dev, f64, replace_blocks
 
 pytestmark = pytest.mark.gpu
 
-# the partition size bench.py uses for the batched-decode workload
-BENCH_PARTITION = 1024
+# the partition size bench.py uses for the batched-decode workload (unsplit, longest sequences first)
+BENCH_PARTITION = 0
+# a split setting checked beside it on the same workloads
+SPLIT_PARTITION = 1024
 
 
 @pytest.fixture(autouse=True)
@@ -98,8 +100,8 @@ def test_bf16_shapes(D, bs, H, G):
 def test_batched_decode_recipe_small():
     """The batched-decode recipe with fewer, shorter sequences (several tiles, ragged tails)."""
     case = wl.config2_batched_decode(poison=True, num_seqs=12, len_lo=17, len_hi=1500, extra_blocks=9)
-    check_case(case, 0)
     check_case(case, BENCH_PARTITION)
+    check_case(case, SPLIT_PARTITION)
 
 
 def test_split_sizes_agree():
@@ -110,20 +112,34 @@ def test_split_sizes_agree():
         assert_parity(o, ref, torch.bfloat16)
 
 
-def test_block_permutation_is_bitwise_invariant():
+@pytest.mark.parametrize("P", [BENCH_PARTITION, SPLIT_PARTITION])
+def test_block_permutation_is_bitwise_invariant(P):
     case = wl.config2_batched_decode(num_seqs=6, len_lo=100, len_hi=900, extra_blocks=20)
-    base, base_lse = gpu_decode(case, BENCH_PARTITION)
+    base, base_lse = gpu_decode(case, P)
     for seed in (1, 2):
         k2, v2, bt2 = replace_blocks(case.k_cache, case.v_cache, case.block_table, case.seq_lens, seed)
-        out, lse = gpu_decode(case, BENCH_PARTITION, block_table=bt2, k_cache=k2, v_cache=v2)
+        out, lse = gpu_decode(case, P, block_table=bt2, k_cache=k2, v_cache=v2)
         assert torch.equal(out, base) and torch.equal(lse, base_lse)
 
 
-def test_repeat_runs_are_bitwise_equal():
+@pytest.mark.parametrize("P", [BENCH_PARTITION, SPLIT_PARTITION])
+def test_repeat_runs_are_bitwise_equal(P):
     case = wl.config2_batched_decode(num_seqs=8, len_lo=500, len_hi=3000)
-    a = gpu_decode(case, BENCH_PARTITION)
-    b = gpu_decode(case, BENCH_PARTITION)
+    a = gpu_decode(case, P)
+    b = gpu_decode(case, P)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("lens", [
+    [700] * 9 + [33, 700, 1, 700],                      # ties: the order among equal lengths is by index
+    list(range(1, 200)),                                 # more sequences than the in-kernel ranking handles
+    [5, 4096, 0, 4096, 17],                              # empty sequences rank last
+])
+def test_longest_first_order_keeps_every_output_in_place(lens):
+    """The unsplit path hands sequences to CTAs longest first; each output must still
+    land in its own row."""
+    case = wl.make_decode_case(31, lens, H=16, G=4, D=128, bs=16, dtype=torch.bfloat16, extra_blocks=3, poison=True)
+    check_case(case, 0)
 
 
 def test_empty_sequence_gives_zero_and_neg_inf():
@@ -146,7 +162,7 @@ def test_batched_decode_full_size():
     """64 seqs, lengths U[512, 4096], 32/8 heads, head_dim 128, block 16: every output vs the oracle."""
     case = wl.config2_batched_decode(poison=False)
     check_case(case, BENCH_PARTITION)
-    check_case(case, 0)
+    check_case(case, SPLIT_PARTITION)
 
 
 def test_long_split_decode_full_size_sampled():
