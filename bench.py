@@ -4,9 +4,11 @@
 Workload: batched paged decode in bf16 -- 64 sequences with lengths drawn
 U[512, 4096], 32 query heads over 8 KV heads, head_dim 128, 16-token pages
 placed by a random permutation of the block pool (seeded, synthetic).  One
-step is one pass of the whole decode path over the batch: the split-KV
-partial kernel (block-table walk, paged K/V gather, QK^T, online softmax,
-PV) and the log-sum-exp merge.  The KV cache (604 MB) is larger than L2, and
+step is one pass of the whole decode path over the batch: one decode call
+(block-table walk, paged K/V gather, QK^T, online softmax, PV, finalise),
+unsplit with the longest sequences first (``--partition P`` > 0 times the
+split-KV partial kernel and the log-sum-exp merge instead).  The KV cache
+(604 MB) is larger than L2, and
 L2 is additionally flushed (a 2x-L2 write) between timed steps, outside the
 timed events.
 
@@ -408,7 +410,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel", "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profiled_traffic(), "kernel_ms": kern_avg_ms, "merge_ms": merge_avg_ms,
+                     "traffic": profiled_traffic(), "kernel_ms": kern_avg_ms, "merge_ms": merge_avg_ms if P > 0 else None,
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": world * nbytes * e2e_n / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_n,
