@@ -20,3 +20,4 @@ from .attention import (  # noqa: F401
     split_partials,
 )
 from .cache_write import mla_reshape_and_cache, reshape_and_cache  # noqa: F401,E402
+from .prefix_cache import block_hashes, lookup_or_allocate, mix64  # noqa: F401,E402
