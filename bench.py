@@ -16,9 +16,10 @@ timed events.
 
 The line also carries ``workloads``: the tiny fp32 decode, the long-context
 split-KV decode (GB/s), the chunked prefill mixed with decodes (TFLOP/s against
-the measured bf16 peak), the MLA decode (TFLOP/s and GB/s) and the paged KV
-write of the chunked-prefill step's new rows (GB/s), each timed the same way as
-one call of its entry point.
+the measured bf16 peak), the MLA decode (TFLOP/s and GB/s), the paged KV
+write of the chunked-prefill step's new rows (GB/s) and the prefix-cache page
+keys + lookup over 4096 prompts sharing system prompts (tokens/s), each timed
+the same way as one call of its entry point.
 
 ``value`` is decode KV GB/s: the algorithmic bytes of a step (every cached
 token's K and V row for its KV head, the queries, outputs, block-table
@@ -561,6 +562,63 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
                            "note": "the chunked-prefill step's new K/V rows scattered into their pages"}
         del key, value, kc, vc, slots, c
         torch.cuda.empty_cache()
+    if "pfx" in names:
+        # prefix-cache page keys + lookup-or-allocate over a batch of prompts sharing system prompts
+        c = wl.prefix_workload()
+        cap = 1 << 17
+        table = pa.prefix_table_alloc(cap, dev)
+        tok, cut, cup = (torch.from_numpy(x).to(dev) for x in (c.tokens, c.cu_tokens, c.cu_pages))
+        stack = torch.from_numpy(c.free_stack).to(dev)
+        count0 = torch.tensor([c.num_pages], dtype=torch.int32, device=dev)
+        count = count0.clone()
+        ref = torch.zeros(c.num_pages, dtype=torch.int32, device=dev)
+        keys = torch.empty(c.total_pages, dtype=torch.int64, device=dev)
+        pages = torch.empty(c.total_pages, dtype=torch.int32, device=dev)
+        hits = torch.empty(c.total_pages, dtype=torch.uint8, device=dev)
+        ws = torch.empty(pa.metis_prefix_lookup_workspace_bytes(c.total_pages), dtype=torch.uint8, device=dev)
+
+        def hashes():
+            pa.metis_prefix_block_hashes(tok, cut, cup, c.block_size, c.total_pages, keys_out=keys)
+
+        def lookup():
+            pa.metis_prefix_table_init(*table)
+            count.copy_(count0)
+            pa.metis_prefix_lookup(keys, table, stack, count, ref, pages_out=pages, hits_out=hits, workspace=ws)
+
+        def whole():
+            hashes()
+            lookup()
+
+        def as_graph(fn):
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fn()
+            torch.cuda.current_stream().wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):  # the calls above launch on the current (capturing) stream
+                fn()
+            torch.cuda.synchronize()
+            return g
+
+        # device time of the step: each piece captured as a CUDA graph and replayed
+        # (eager calls are bound by the host's issue rate at these sizes)
+        med, _ = _time_calls(as_graph(whole).replay, reps, flush, stream)
+        hmed, _ = _time_calls(as_graph(hashes).replay, reps, flush, stream)
+        lmed, _ = _time_calls(as_graph(lookup).replay, reps, flush, stream)
+        emed, _ = _time_calls(whole, reps, flush, stream)
+        torch.cuda.synchronize()
+        hit_rate = float(hits.float().mean().item())
+        res["prefix_lookup"] = {"ms": med, "hash_ms": hmed, "lookup_ms": lmed, "eager_ms": emed,
+                                "tokens": c.num_tokens, "prompts": c.num_seqs, "pages": c.total_pages,
+                                "tokens_per_s": c.num_tokens / (med * 1e-3),
+                                "pages_per_s": c.total_pages / (med * 1e-3), "hit_rate": hit_rate,
+                                "launches": 7,
+                                "note": "one step as a CUDA graph: table reset, stack depth reset, page keys of "
+                                        "every full page, lookup-or-allocate in batch order; eager_ms: the same "
+                                        "step issued call by call from Python"}
+        del table, tok, cut, cup, stack, count0, count, ref, keys, pages, hits, ws, c
+        torch.cuda.empty_cache()
     if "c5" in names:
         c = wl.config5_mla_decode()
         t = [x.to(dev) for x in (c.q, c.kv_cache, c.block_table, c.seq_lens)]
@@ -593,8 +651,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=PARTITION)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workloads", default="c1,c3,c4,c5,kvw",
-                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw; empty: none)")
+    ap.add_argument("--workloads", default="c1,c3,c4,c5,kvw,pfx",
+                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw,pfx; "
+                         "empty: none)")
     ap.add_argument("--workload-reps", type=int, default=20)
     ap.add_argument("--ramp-steps", type=int, default=None,
                     help="untimed steps before warm-up (default: about one second of steps)")

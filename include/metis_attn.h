@@ -68,6 +68,9 @@ extern "C" {
 #define METIS_STATUS_SEQ_TOO_LONG  2u  /* seq_lens[s] > max_blocks * block_size or > max_seq_len */
 #define METIS_STATUS_WAIT_TIMEOUT  4u  /* a pipeline wait gave up (a library bug) */
 #define METIS_STATUS_BAD_Q_LEN     8u  /* prefill: q_len > seq_len or a negative q_len */
+#define METIS_STATUS_TABLE_FULL   16u  /* prefix lookup: a key found no free table slot */
+#define METIS_STATUS_OUT_OF_PAGES 32u  /* prefix lookup: a new key found the free stack empty */
+#define METIS_STATUS_BAD_OFFSETS  64u  /* page keys: cu_pages asks for a page past its sequence's tokens */
 
 /*
  * metis_paged_attn_decode -- one query token per sequence over its pages
@@ -313,6 +316,82 @@ int metis_reshape_and_cache(const void* key, const void* value, void* k_cache, v
 int metis_mla_reshape_and_cache(const void* kv_c, const void* k_pe, void* kv_cache,
                                 const int64_t* slot_mapping, int num_tokens, int d_latent, int d_rope,
                                 int block_size, int num_blocks, void* stream);
+
+/*
+ * Prefix cache: page keys and lookup-or-allocate.  A new prompt reuses the KV
+ * pages of an earlier prompt with the same leading tokens (vllm-metis 0.1.0
+ * page, "How the model maps onto vLLM", "Caches": vLLM's cache manager runs
+ * prefix caching; "Status": most of a repeated prompt's tokens come from the
+ * cache).  The pages are those of the block table (vllm-metal article,
+ * section 4).
+ *
+ * metis_prefix_block_hashes -- one chained 64-bit key per FULL page:
+ *   local_b = fold over the page's tokens t of  x = mix64(x ^ (uint32)t),
+ *             starting from x = 0x9E3779B97F4A7C15
+ *   key_b   = mix64(key_{b-1} ^ local_b), key_{-1} = 0; a key of 0 becomes 1
+ * with mix64 splitmix64's output function (Steele, Lea and Flood 2014), so a
+ * key names a page's tokens and every token before them.
+ *
+ *   token_ids  int32 [cu_tokens[num_seqs]]: the sequences' tokens, concatenated
+ *   cu_tokens  int32 [num_seqs + 1]: token offsets (cu_tokens[0] = 0)
+ *   cu_pages   int32 [num_seqs + 1]: key offsets; cu_pages[s + 1] - cu_pages[s]
+ *              must equal (cu_tokens[s + 1] - cu_tokens[s]) / block_size (the
+ *              partial last page has no key) -- the caller computes it on the
+ *              host, where it sizes keys_out
+ *   total_pages  cu_pages[num_seqs]
+ *   keys_out   uint64 [total_pages], sequence-major
+ * A page that cu_pages places past its sequence's tokens is not read: its key
+ * is 0 and METIS_STATUS_BAD_OFFSETS is set.
+ * Device pointers, caller-owned; index arrays 4-byte aligned, keys_out
+ * 8-byte.  num_seqs == 0 or total_pages == 0 is a successful no-op.
+ *
+ * metis_prefix_table_init -- empty an open-addressing table of `capacity`
+ * slots (a power of two): table_keys[i] = 0 (0 is never a key),
+ * table_pages[i] = -1, table_claim[i] = INT_MAX.  The three arrays are
+ * caller-owned device memory that persists across lookups; table_claim is
+ * scratch the lookup leaves at INT_MAX.
+ *
+ * metis_prefix_lookup -- look the n keys up in order (sequence-major, as
+ * metis_prefix_block_hashes writes them), with the result of one-at-a-time
+ * processing:
+ *   a key whose slot holds a page p >= 0 is a hit: pages_out = p,
+ *     hits_out = 1, refcount[p] += 1;
+ *   otherwise the key is new; the FIRST new occurrence of a key in the batch
+ *     takes the page on top of the free stack (free_stack[*free_count - 1],
+ *     then the one below ...): pages_out = that page, hits_out = 0,
+ *     refcount[page] = 1, and the slot keeps the page; later occurrences in
+ *     the same batch are hits on it;
+ *   a new key with the stack empty gets pages_out = -1, hits_out = 0 and
+ *     sets METIS_STATUS_OUT_OF_PAGES; its slot keeps page -1, which later
+ *     lookups treat as absent.
+ *   keys         uint64 [n], none 0
+ *   table_*      as metis_prefix_table_init left them (or earlier lookups)
+ *   free_stack   int32 [free_capacity]: free page ids, the top at the end
+ *   free_count   int32 (one device value): pages on the stack; decremented by
+ *                the pages taken (read clamped to [0, free_capacity])
+ *   refcount     int32 [num_pages]
+ *   pages_out    int32 [n];  hits_out  uint8 [n]
+ *   workspace    metis_prefix_lookup_workspace_bytes(n) bytes, 256-byte aligned
+ * A key that finds no free table slot (probing wraps around) gets page -1 and
+ * sets METIS_STATUS_TABLE_FULL; a stack entry outside [0, num_pages) is not
+ * used and sets METIS_STATUS_BAD_BLOCK_ID.  Keeping the table at most half full
+ * is the caller's job.  Device pointers, caller-owned; uint64 arrays 8-byte and
+ * int32 arrays 4-byte aligned.  Returns METIS_OK or METIS_E_* (nothing
+ * launched); n == 0 is a successful no-op.  All three calls are asynchronous on
+ * `stream`, allocate nothing, and can be captured in a CUDA graph.
+ */
+int metis_prefix_block_hashes(const int32_t* token_ids, const int32_t* cu_tokens, const int32_t* cu_pages,
+                              int num_seqs, int block_size, int total_pages, uint64_t* keys_out, void* stream);
+
+int metis_prefix_table_init(uint64_t* table_keys, int32_t* table_pages, int32_t* table_claim, int capacity,
+                            void* stream);
+
+size_t metis_prefix_lookup_workspace_bytes(int n);
+
+int metis_prefix_lookup(const uint64_t* keys, int n, uint64_t* table_keys, int32_t* table_pages,
+                        int32_t* table_claim, int capacity, const int32_t* free_stack, int free_capacity,
+                        int32_t* free_count, int32_t* refcount, int num_pages, int32_t* pages_out,
+                        uint8_t* hits_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * metis_read_status -- the device status word (METIS_STATUS_* bits, OR-ed

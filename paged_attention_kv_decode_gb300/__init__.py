@@ -13,8 +13,11 @@ from ._binding import (  # noqa: F401
     METIS_F32,
     SIGNATURES,
     STATUS_BAD_BLOCK_ID,
+    STATUS_BAD_OFFSETS,
     STATUS_BAD_Q_LEN,
+    STATUS_OUT_OF_PAGES,
     STATUS_SEQ_TOO_LONG,
+    STATUS_TABLE_FULL,
     STATUS_WAIT_TIMEOUT,
     MetisError,
     load_library,
@@ -30,6 +33,11 @@ from ._binding import (  # noqa: F401
     metis_paged_attn_decode_partials,
     metis_paged_attn_prefill_chunk,
     metis_prefill_workspace_bytes,
+    metis_prefix_block_hashes,
+    metis_prefix_lookup,
+    metis_prefix_lookup_workspace_bytes,
+    metis_prefix_table_init,
+    prefix_table_alloc,
     split_workspace_views,
     metis_read_status,
     metis_reshape_and_cache,

@@ -27,6 +27,9 @@ STATUS_BAD_BLOCK_ID = 1
 STATUS_SEQ_TOO_LONG = 2
 STATUS_WAIT_TIMEOUT = 4
 STATUS_BAD_Q_LEN = 8
+STATUS_TABLE_FULL = 16
+STATUS_OUT_OF_PAGES = 32
+STATUS_BAD_OFFSETS = 64
 
 _ERRORS = {
     -1: "METIS_E_NULL",
@@ -74,6 +77,10 @@ SIGNATURES = {
     "metis_version": (_i, []),
     "metis_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "metis_mla_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "metis_prefix_block_hashes": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "metis_prefix_table_init": (_i, [_vp, _vp, _vp, _i, _vp]),
+    "metis_prefix_lookup_workspace_bytes": (_sz, [_i]),
+    "metis_prefix_lookup": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -402,3 +409,93 @@ def metis_mla_reshape_and_cache(kv_c: torch.Tensor, k_pe: torch.Tensor, kv_cache
         raise ValueError("inconsistent shapes")
     _check(lib.metis_mla_reshape_and_cache(_ptr(kv_c), _ptr(k_pe), _ptr(kv_cache), _ptr(slot_mapping), N, dl, dr,
                                            bs, nb, _stream(stream)))
+
+
+def metis_prefix_block_hashes(token_ids: torch.Tensor, cu_tokens: torch.Tensor, cu_pages: torch.Tensor,
+                              block_size: int, total_pages: int, keys_out: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """Chained key of every full page (int64 ``[total_pages]`` holding the uint64 bit
+    pattern).  ``cu_pages`` (int32 ``[S + 1]``) and ``total_pages`` are the caller's:
+    sequence s has ``(cu_tokens[s+1] - cu_tokens[s]) // block_size`` keys."""
+    lib = load_library()
+    _cuda("token_ids", token_ids, dtype=torch.int32, ndim=1)
+    _cuda("cu_tokens", cu_tokens, dtype=torch.int32, ndim=1)
+    _cuda("cu_pages", cu_pages, dtype=torch.int32, ndim=1)
+    S = cu_tokens.shape[0] - 1
+    if cu_pages.shape[0] != S + 1:
+        raise ValueError("cu_tokens and cu_pages must both have num_seqs + 1 entries")
+    if keys_out is None:
+        keys_out = torch.empty(total_pages, dtype=torch.int64, device=token_ids.device)
+    _cuda("keys_out", keys_out, dtype=torch.int64, ndim=1)
+    if keys_out.shape[0] < total_pages:
+        raise ValueError("keys_out is shorter than total_pages")
+    _check(lib.metis_prefix_block_hashes(_ptr(token_ids), _ptr(cu_tokens), _ptr(cu_pages), S, int(block_size),
+                                         int(total_pages), _ptr(keys_out), _stream(stream)))
+    return keys_out
+
+
+def metis_prefix_table_init(table_keys: torch.Tensor, table_pages: torch.Tensor, table_claim: torch.Tensor,
+                            stream=None) -> None:
+    """Empty the open-addressing table (int64 keys, int32 pages, int32 claim; one
+    power-of-two capacity); asynchronous."""
+    lib = load_library()
+    _cuda("table_keys", table_keys, dtype=torch.int64, ndim=1)
+    _cuda("table_pages", table_pages, dtype=torch.int32, ndim=1)
+    _cuda("table_claim", table_claim, dtype=torch.int32, ndim=1)
+    cap = table_keys.shape[0]
+    if table_pages.shape[0] != cap or table_claim.shape[0] != cap:
+        raise ValueError("the three table arrays must have one capacity")
+    _check(lib.metis_prefix_table_init(_ptr(table_keys), _ptr(table_pages), _ptr(table_claim), cap,
+                                       _stream(stream)))
+
+
+def prefix_table_alloc(capacity: int, device="cuda", stream=None):
+    """Allocate and empty a table of ``capacity`` slots; returns ``(keys, pages, claim)``."""
+    keys = torch.empty(capacity, dtype=torch.int64, device=device)
+    pages = torch.empty(capacity, dtype=torch.int32, device=device)
+    claim = torch.empty(capacity, dtype=torch.int32, device=device)
+    metis_prefix_table_init(keys, pages, claim, stream)
+    return keys, pages, claim
+
+
+def metis_prefix_lookup_workspace_bytes(n: int) -> int:
+    return int(load_library().metis_prefix_lookup_workspace_bytes(n))
+
+
+def metis_prefix_lookup(keys: torch.Tensor, table, free_stack: torch.Tensor, free_count: torch.Tensor,
+                        refcount: torch.Tensor, pages_out: Optional[torch.Tensor] = None,
+                        hits_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None):
+    """Lookup-or-allocate of ``keys`` (int64 ``[n]``) in ``table`` (the tuple of
+    ``prefix_table_alloc``); ``free_stack`` int32 (top at the end), ``free_count``
+    int32 ``[1]`` and ``refcount`` int32 ``[num_pages]`` are updated in place.
+    Returns ``(pages int32 [n], hits uint8 [n])``; asynchronous."""
+    lib = load_library()
+    table_keys, table_pages, table_claim = table
+    _cuda("keys", keys, dtype=torch.int64, ndim=1)
+    _cuda("table_keys", table_keys, dtype=torch.int64, ndim=1)
+    _cuda("table_pages", table_pages, dtype=torch.int32, ndim=1)
+    _cuda("table_claim", table_claim, dtype=torch.int32, ndim=1)
+    _cuda("free_stack", free_stack, dtype=torch.int32, ndim=1)
+    _cuda("free_count", free_count, dtype=torch.int32, ndim=1)
+    _cuda("refcount", refcount, dtype=torch.int32, ndim=1)
+    n = keys.shape[0]
+    dev = keys.device
+    if pages_out is None:
+        pages_out = torch.empty(n, dtype=torch.int32, device=dev)
+    if hits_out is None:
+        hits_out = torch.empty(n, dtype=torch.uint8, device=dev)
+    _cuda("pages_out", pages_out, dtype=torch.int32, ndim=1)
+    _cuda("hits_out", hits_out, dtype=torch.uint8, ndim=1)
+    if pages_out.shape[0] < n or hits_out.shape[0] < n:
+        raise ValueError("pages_out / hits_out are shorter than keys")
+    need = metis_prefix_lookup_workspace_bytes(n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _cuda("workspace", workspace, dtype=torch.uint8, ndim=1)
+    cap = table_keys.shape[0]
+    _check(lib.metis_prefix_lookup(_ptr(keys), n, _ptr(table_keys), _ptr(table_pages), _ptr(table_claim), cap,
+                                   _ptr(free_stack), free_stack.shape[0], _ptr(free_count), _ptr(refcount),
+                                   refcount.shape[0], _ptr(pages_out), _ptr(hits_out), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)))
+    return pages_out, hits_out

@@ -89,6 +89,8 @@ extern "C" int metis_read_status(uint32_t* status_out, int clear) {
   if (rc) return rc;
   rc = metis::cache_status(&bits, clear);
   if (rc) return rc;
+  rc = metis::prefix_status(&bits, clear);
+  if (rc) return rc;
   *status_out = bits;
   return METIS_OK;
 }

@@ -64,5 +64,6 @@ int decode_status(uint32_t* bits, int clear);
 int prefill_status(uint32_t* bits, int clear);
 int mla_status(uint32_t* bits, int clear);
 int cache_status(uint32_t* bits, int clear);
+int prefix_status(uint32_t* bits, int clear);
 
 }  // namespace metis

@@ -335,6 +335,62 @@ def config5_mla_decode(poison: bool = False, num_seqs: int = 128, median: int = 
                          extra_blocks=extra_blocks, name="c5_mla_decode_bf16", rng=rng)
 
 
+class PrefixCase:
+    """Prompts for the prefix-cache lookup: tokens, offsets and a free-page stack.
+
+    ``tokens`` int32 ``[T]`` (the prompts concatenated), ``cu_tokens`` /
+    ``cu_pages`` int32 ``[S + 1]`` (token and full-page offsets), ``free_stack``
+    int32 ``[num_pages]`` (a seeded permutation of the page ids, top at the end).
+    """
+
+    def __init__(self, name, tokens, cu_tokens, block_size, num_pages, free_stack):
+        self.name = name
+        self.tokens = tokens
+        self.cu_tokens = cu_tokens
+        self.block_size = block_size
+        lens = np.diff(cu_tokens)
+        self.cu_pages = np.concatenate([[0], np.cumsum(lens // block_size)]).astype(np.int32)
+        self.total_pages = int(self.cu_pages[-1])
+        self.num_pages = num_pages
+        self.free_stack = free_stack
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.cu_tokens) - 1
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.cu_tokens[-1])
+
+
+def make_prefix_case(seed: int, num_seqs: int, num_prefixes: int, prefix_lo: int, prefix_hi: int, suffix_lo: int,
+                     suffix_hi: int, bs: int, num_pages: int, vocab: int = 32000, name: str = "prefix") -> PrefixCase:
+    """Each prompt = one of ``num_prefixes`` shared system prompts (lengths uniform in
+    [prefix_lo, prefix_hi]) followed by its own suffix (uniform in [suffix_lo, suffix_hi]);
+    token ids uniform in [0, vocab).  Draw order: prefix lengths, prefix tokens, the prefix
+    choice per prompt, suffix lengths, suffix tokens, then the free-stack permutation."""
+    rng = _rng(seed)
+    plens = rng.integers(prefix_lo, prefix_hi + 1, size=num_prefixes)
+    prefixes = [rng.integers(0, vocab, size=int(n), dtype=np.int64).astype(np.int32) for n in plens]
+    choice = rng.integers(0, num_prefixes, size=num_seqs)
+    slens = rng.integers(suffix_lo, suffix_hi + 1, size=num_seqs)
+    parts = []
+    for s in range(num_seqs):
+        parts.append(prefixes[choice[s]])
+        parts.append(rng.integers(0, vocab, size=int(slens[s]), dtype=np.int64).astype(np.int32))
+    tokens = np.concatenate(parts) if parts else np.zeros(0, np.int32)
+    lens = plens[choice] + slens
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    stack = rng.permutation(num_pages).astype(np.int32)
+    return PrefixCase(name, tokens, cu, bs, num_pages, stack)
+
+
+def prefix_workload(num_seqs: int = 4096) -> PrefixCase:
+    """4096 prompts of 640-768 tokens sharing 16 system prompts of 576-640 tokens, block 16,
+    a pool of 262144 pages (the repeated-prompt shape of the vllm-metis status report)."""
+    return make_prefix_case(1006, num_seqs, 16, 576, 640, 32, 160, 16, 262144, name="prefix_lookup_4096x700")
+
+
 CONFIGS = {
     "c1": config1_tiny_decode,
     "c2": config2_batched_decode,

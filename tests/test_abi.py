@@ -219,3 +219,54 @@ def test_mla_reshape_and_cache_rejects(lib, kw, code):
     rc = lib.metis_mla_reshape_and_cache(vp(a["kv_c"]), vp(a["k_pe"]), vp(a["kv"]), vp(a["slots"]), a["n"], a["dl"],
                                          a["dr"], a["bs"], a["nb"], None)
     assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=-1), -2), (dict(total=-1), -2), (dict(tok=None), -1), (dict(keys=None), -1), (dict(bs=0), -2),
+    (dict(tok=FAKE + 2), -4), (dict(cup=FAKE + 1), -4), (dict(keys=FAKE + 4), -4),
+])
+def test_prefix_block_hashes_rejects(lib, kw, code):
+    a = dict(tok=FAKE, cut=FAKE, cup=FAKE, S=4, bs=16, total=8, keys=FAKE)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.metis_prefix_block_hashes(vp(a["tok"]), vp(a["cut"]), vp(a["cup"]), a["S"], a["bs"], a["total"],
+                                       vp(a["keys"]), None)
+    assert rc == code, pa.metis_last_error()
+
+
+def test_prefix_block_hashes_empty_is_a_no_op(lib):
+    vp = ctypes.c_void_p
+    assert lib.metis_prefix_block_hashes(vp(FAKE), vp(FAKE), vp(FAKE), 0, 16, 8, vp(FAKE), None) == 0
+    assert lib.metis_prefix_block_hashes(None, None, None, 4, 16, 0, None, None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cap=0), -2), (dict(cap=6), -2), (dict(keys=None), -1), (dict(keys=FAKE + 4), -4), (dict(claim=FAKE + 2), -4),
+])
+def test_prefix_table_init_rejects(lib, kw, code):
+    a = dict(keys=FAKE, pages=FAKE, claim=FAKE, cap=1024)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    assert lib.metis_prefix_table_init(vp(a["keys"]), vp(a["pages"]), vp(a["claim"]), a["cap"], None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), -2), (dict(keys=None), -1), (dict(fc=None), -1), (dict(cap=100), -2), (dict(fcap=-1), -2),
+    (dict(npages=0), -2), (dict(keys=FAKE + 4), -4), (dict(po=FAKE + 2), -4), (dict(ws=None), -5),
+    (dict(ws_bytes=256), -5), (dict(ws=FAKE + 16), -5),
+])
+def test_prefix_lookup_rejects(lib, kw, code):
+    a = dict(keys=FAKE, n=16, tk=FAKE, tp=FAKE, tc=FAKE, cap=1024, fs=FAKE, fcap=64, fc=FAKE, rc=FAKE, npages=64,
+             po=FAKE, ho=FAKE, ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.metis_prefix_lookup(vp(a["keys"]), a["n"], vp(a["tk"]), vp(a["tp"]), vp(a["tc"]), a["cap"], vp(a["fs"]),
+                                 a["fcap"], vp(a["fc"]), vp(a["rc"]), a["npages"], vp(a["po"]), vp(a["ho"]),
+                                 vp(a["ws"]), a["ws_bytes"], None)
+    assert rc == code, pa.metis_last_error()
+
+
+def test_prefix_lookup_empty_and_workspace(lib):
+    assert lib.metis_prefix_lookup(None, 0, None, None, None, 0, None, 0, None, None, 0, None, None, None, 0, None) == 0
+    assert lib.metis_prefix_lookup_workspace_bytes(0) == 0
+    assert lib.metis_prefix_lookup_workspace_bytes(16) >= 16 * 5
