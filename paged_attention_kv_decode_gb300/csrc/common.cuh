@@ -214,6 +214,19 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return r;
 }
 
+// Warpgroup register reallocation: the four warps of a warpgroup execute the same
+// one.  The registers a block gives up or takes come from its launch allocation
+// (threads x registers per thread at launch), so the targets must add up to at
+// most that.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // max of three floats in one instruction
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;

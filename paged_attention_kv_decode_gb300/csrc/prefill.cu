@@ -22,6 +22,8 @@
 //                and V tiles (warps 10, 11) into 2-stage rings, each tile's pages
 //                split between two warps (16-token pages make many small boxes,
 //                and one warp alone cannot issue them fast enough)
+//   warps 13..15 idle (they complete the last warpgroup, which gives up
+//                registers to the softmax groups)
 //   warp 12      allocates TMEM (S0 | S1 | O0 | O1, 512 columns); one lane
 //                issues the UMMAs in the order
 //                  PV0_j, QK0_{j+1}, PV1_j, QK1_{j+1}
@@ -29,6 +31,8 @@
 //                other group's products (ping-pong).
 //                  S_w = Q_w K_j^T  (M 128, N 128, K = head_dim)
 //                  O_w += P_w V_j   (M 128, N head_dim, K 128; P_w read from TMEM)
+// Registers: the producer and UMMA warpgroups drop to kRegsLow so that each
+// softmax thread holds its row's 128 scores at once (one TMEM read per tile).
 // Softmax: running max in log2 units, P = exp2(S - m) written back as bf16
 // pairs over its own S columns; O is rescaled in TMEM only when the max grows
 // by more than 2^8.  Because QK_w_{j+1} is issued after PV_w_j, "S_w_j landed"
@@ -49,8 +53,13 @@ namespace metis {
 
 __device__ unsigned int g_status_prefill = 0;
 
-constexpr int kPfThreads = 416;   // 2 softmax groups + 4 TMA warps + MMA warp
+constexpr int kPfThreads = 512;   // 2 softmax groups + 4 TMA warps + MMA warp + 3 idle warps
 constexpr int kMmaWarp = 12;
+constexpr int kRegsLaunch = 65536 / kPfThreads;  // 128: the block takes the whole register file
+constexpr int kRegsSoftmax = 208;                 // warpgroups 0, 1
+constexpr int kRegsLow = 48;                      // warpgroups 2, 3
+static_assert(128 * (2 * kRegsSoftmax + 2 * kRegsLow) <= kPfThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr int kKStages = 3;       // K ring depth (V ring: 2)
 constexpr int kKvTile = 128;      // tokens per K/V tile
 constexpr int kRows = 128;        // query rows per tile
@@ -249,6 +258,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
 
   if (warp >= 8 && warp < kMmaWarp) {
     // ------------------------------------------------------------ TMA producers
+    regs_dec<kRegsLow>();
     const int pw = warp - 8;
     const bool is_k = pw < 2;
     const int part = pw & 1;                   // which half of each tile's pages
@@ -301,6 +311,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ UMMA issuer
+    regs_dec<kRegsLow>();
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kRows, kKvTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kRows, D, false, true);
     const int nw[2] = {n0, n1};
@@ -394,8 +405,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       __syncwarp();
       mbar_wait(drain, 0, &g_status_prefill);
     }
+  } else if (warp > kMmaWarp) {
+    regs_dec<kRegsLow>();  // idle: give the registers to the softmax groups
   } else {
     // ------------------------------------------------------------ softmax groups
+    regs_inc<kRegsSoftmax>();
     const int w = warp >> 2;                    // query tile of this group
     const int nkv = w ? n1 : n0;
     const int row = (warp & 3) * 32 + lane;
@@ -426,25 +440,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       // Visible keys of this row in this tile form a prefix: t <= p_row.
       const int vis = tok0 + kKvTile - 1 > p_min ? min(max(p_row - tok0 + 1, 0), kKvTile) : kKvTile;
       const bool lean = vis == kKvTile && sgn > 0.f;   // the common case: no mask, positive scale
-      // pass 1: row max over the 128 scores, 64 columns at a time
+      // the row's 128 scores, read once
+      uint32_t sv[kKvTile];
+#pragma unroll
+      for (int c = 0; c < kKvTile; c += 32) tmem_ld32(s_tmem + c, sv + c);
+      tmem_ld_wait();
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      if (lean) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[64];
-        tmem_ld32(s_tmem + half * 64, sv);
-        tmem_ld32(s_tmem + half * 64 + 32, sv + 32);
-        tmem_ld_wait();
-        if (lean) {
+        for (int c = 0; c < kKvTile; c += 2)
+          mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+      } else {
 #pragma unroll
-          for (int c = 0; c < 64; c += 2)
-            mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            mx[c & 7] = fmaxf(mx[c & 7], half * 64 + c < vis ? __uint_as_float(sv[c]) * sgn : -INFINITY);
-        }
+        for (int c = 0; c < kKvTile; ++c)
+          mx[c & 7] = fmaxf(mx[c & 7], c < vis ? __uint_as_float(sv[c]) * sgn : -INFINITY);
       }
       const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
@@ -467,41 +478,33 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         }
       }
       l_run *= alpha;
-      // pass 2: P = exp2(s * |sl2| - m) as bf16 pairs (even token in the low half), 64 tokens
-      // at a time, over the first 64 columns of S_w (columns already consumed)
+      // P = exp2(s * |sl2| - m) as bf16 pairs (even token in the low half), packed in
+      // place into sv[0, 64) and stored over the first 64 columns of S_w
       const float neg_m = -m_run;
       uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // row sums, as packed pairs
       const uint64_t asl2_2 = f2_pack(asl2, asl2), neg_m2 = f2_pack(neg_m, neg_m);
+      if (lean) {
+        // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[64];
-        tmem_ld32(s_tmem + half * 64, sv);
-        tmem_ld32(s_tmem + half * 64 + 32, sv + 32);
-        tmem_ld_wait();
-        uint32_t pk[32];
-        if (lean) {
-          // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
-            const float e0 = exp2_approx(x0);
-            const float e1 = exp2_approx(x1);
-            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
-            pk[c >> 1] = pack_bf16x2(e0, e1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const int t = half * 64 + c;
-            const float e0 = t < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
-            const float e1 = t + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
-            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
-            pk[c >> 1] = pack_bf16x2(e0, e1);
-          }
+        for (int c = 0; c < kKvTile; c += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
+          const float e0 = exp2_approx(x0);
+          const float e1 = exp2_approx(x1);
+          ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
+          sv[c >> 1] = pack_bf16x2(e0, e1);
         }
-        tmem_st32(s_tmem + half * 32, pk);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kKvTile; c += 2) {
+          const float e0 = c < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
+          const float e1 = c + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
+          ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
+          sv[c >> 1] = pack_bf16x2(e0, e1);
+        }
       }
+      tmem_st32(s_tmem, sv);
+      tmem_st32(s_tmem + 32, sv + 32);
       float ls[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) f2_unpack(ls2[i], ls[2 * i], ls[2 * i + 1]);
@@ -594,6 +597,18 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
   auto kern = prefill_bf16_kernel<D>;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem, &done);
   if (rc) return rc;
+  // the warpgroups' register targets draw on the launch allocation: refuse to launch
+  // a build whose allocation is smaller (the raising warps would wait forever)
+  static int regs_checked = 0;
+  if (!regs_checked) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kern));
+    if (e != cudaSuccess) return fail(METIS_E_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+    if (fa.numRegs < kRegsLaunch)
+      return fail(METIS_E_CUDA, "prefill kernel built with %d registers per thread, %d needed", fa.numRegs,
+                  kRegsLaunch);
+    regs_checked = 1;
+  }
   return launch_dependent(kern, dim3((unsigned)(max_items * p.G)), dim3(kPfThreads), smem, st,
                           "prefill_bf16_kernel launch", tmQ, tmK, tmV, p);
 }
