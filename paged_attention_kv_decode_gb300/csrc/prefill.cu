@@ -18,12 +18,12 @@
 //
 //   warps 0..3   softmax of query tile 0, one row (TMEM lane) per thread
 //   warps 4..7   softmax of query tile 1
-//   warps 8..11  TMA producers: both query tiles once, then K tiles (warps 8, 9)
-//                and V tiles (warps 10, 11) into 2-stage rings, each tile's pages
+//   warps 8..11  TMA producers: K tiles (warps 8, 9) and V tiles (warps 10, 11)
+//                into 3- and 2-stage rings, each tile's pages
 //                split between two warps (16-token pages make many small boxes,
 //                and one warp alone cannot issue them fast enough)
-//   warps 13..15 idle (they complete the last warpgroup, which gives up
-//                registers to the softmax groups)
+//   warp 13      query loader; warp 14 hands out the units; warp 15 idle (the
+//                last warpgroup gives up registers to the softmax groups)
 //   warp 12      allocates TMEM (S0 | S1 | O0 | O1, 512 columns); one lane
 //                issues the UMMAs in the order
 //                  PV0_j, QK0_{j+1}, PV1_j, QK1_{j+1}
@@ -31,15 +31,21 @@
 //                other group's products (ping-pong).
 //                  S_w = Q_w K_j^T  (M 128, N 128, K = head_dim)
 //                  O_w += P_w V_j   (M 128, N head_dim, K 128; P_w read from TMEM)
-// Registers: the producer and UMMA warpgroups drop to kRegsLow so that each
+// Registers: the producer and UMMA warpgroups drop to kRegsProd / kRegsMma so that each
 // softmax thread holds its row's 128 scores at once (one TMEM read per tile).
 // Softmax: running max in log2 units, P = exp2(S - m) written back as bf16
 // pairs over its own S columns; O is rescaled in TMEM only when the max grows
 // by more than 2^8.  Because QK_w_{j+1} is issued after PV_w_j, "S_w_j landed"
 // already implies "PV_w_{j-1} finished", so the rescale never waits.
 //
-// A small schedule kernel first lists the (sequence, query-tile pair) items
-// heaviest first, so the grid has no idle CTAs.
+// Persistent mixed batch: a small schedule kernel lists the (sequence,
+// query-tile pair) items heaviest first -- chunks and single-token decodes in one
+// list -- and one CTA per SM takes units (item, KV head) from that list as it
+// goes (warp 14 claims the next one with an atomic and publishes it to the other
+// warps through a two-slot ring).  Every role keeps its ring and barrier counters
+// running across units, so the next unit's queries (warp 13, once the current
+// unit's last QK has completed) and K/V tiles stream in while the current unit's
+// last softmax, PV and epilogue drain.
 #include <math.h>
 
 #include <algorithm>
@@ -55,10 +61,17 @@ __device__ unsigned int g_status_prefill = 0;
 
 constexpr int kPfThreads = 512;   // 2 softmax groups + 4 TMA warps + MMA warp + 3 idle warps
 constexpr int kMmaWarp = 12;
+constexpr int kUnitReaders = 14;  // warps 0..13 read every unit from the unit ring
 constexpr int kRegsLaunch = 65536 / kPfThreads;  // 128: the block takes the whole register file
-constexpr int kRegsSoftmax = 208;                 // warpgroups 0, 1
-constexpr int kRegsLow = 48;                      // warpgroups 2, 3
-static_assert(128 * (2 * kRegsSoftmax + 2 * kRegsLow) <= kPfThreads * kRegsLaunch,
+#ifndef PF_REGS_SOFTMAX
+#define PF_REGS_SOFTMAX 216
+#define PF_REGS_PROD 40
+#define PF_REGS_MMA 40
+#endif
+constexpr int kRegsSoftmax = PF_REGS_SOFTMAX;  // warpgroups 0, 1: softmax
+constexpr int kRegsProd = PF_REGS_PROD;        // warpgroup 2: K/V producers
+constexpr int kRegsMma = PF_REGS_MMA;          // warpgroup 3: UMMA issuer, query loader, idle warps
+static_assert(128 * (2 * kRegsSoftmax + kRegsProd + kRegsMma) <= kPfThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 constexpr int kKStages = 3;       // K ring depth (V ring: 2)
 constexpr int kKvTile = 128;      // tokens per K/V tile
@@ -74,6 +87,7 @@ struct PrefillParams {
   float* lse_out;
   const int4* items;
   const int* item_count;
+  int* unit_head;   // next unit to hand out (the schedule kernel zeroes it)
   int S, T, H, G, r, Tq, bs, max_blocks, num_blocks, cap;
   float scale_log2;
 };
@@ -176,12 +190,36 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
       items[rank] = me;
     }
   }
-  if (tid == 0) *count = total;
+  if (tid == 0) {
+    *count = total;
+    *p.unit_head = 0;
+  }
 }
 
 // ---------------------------------------------------------------------------
-// main kernel
+// main kernel (persistent: one CTA per SM walks the work list)
 // ---------------------------------------------------------------------------
+// One unit of work as every role sees it: query-tile pair `pair` of sequence s,
+// KV head g.  Each role derives it from the schedule's list on its own.
+struct PfUnit {
+  int s, pair, g, L, q_len, n0, n1, n_kv, q0, n_pages;
+};
+
+__device__ __forceinline__ bool pf_unit(const PrefillParams& p, int u, bool flag, PfUnit& it) {
+  const int item_idx = u / p.G;
+  it.g = u - item_idx * p.G;
+  const int4 v = p.items[item_idx];
+  it.s = v.x;
+  it.pair = v.y;
+  pf_lengths(p, it.s, it.L, it.q_len, flag && it.g == 0);
+  it.n0 = pf_kv_tiles(it.L, it.q_len, 2 * it.pair, p.Tq);      // K/V tiles of query tile 0
+  it.n1 = pf_kv_tiles(it.L, it.q_len, 2 * it.pair + 1, p.Tq);  // ... of query tile 1 (0: no second tile)
+  it.n_kv = max(it.n0, it.n1);
+  it.q0 = p.cu_q_lens[it.s];
+  it.n_pages = (it.L + p.bs - 1) / p.bs;
+  return it.n0 > 0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                        const __grid_constant__ CUtensorMap tmK,
@@ -206,26 +244,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   uint64_t* p_full = bars + 13;   // [2 groups] P_w_j written over S_w (128 arrivals)
   uint64_t* pv_done = bars + 15;  // [2 groups] PV_w_j completed
   uint64_t* drain = bars + 17;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 19);
+  uint64_t* q_free = bars + 18;   // every QK of a unit completed: its query tiles may be replaced
+  uint64_t* unit_full = bars + 19;   // [2] a unit index published
+  uint64_t* unit_empty = bars + 21;  // [2] every consuming warp has read it (kUnitReaders arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 24);
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(bars + 25);  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item_idx = blockIdx.x / p.G, g = blockIdx.x - item_idx * p.G;
-  if (item_idx >= *p.item_count) return;
-  const int4 it = p.items[item_idx];
-  const int s = it.x, pair = it.y;
-  int L, q_len;
-  pf_lengths(p, s, L, q_len, threadIdx.x == 0);
-  const int n0 = pf_kv_tiles(L, q_len, 2 * pair, p.Tq);      // K/V tiles of query tile 0
-  const int n1 = pf_kv_tiles(L, q_len, 2 * pair + 1, p.Tq);  // ... of query tile 1 (0: no second tile)
-  if (n0 <= 0) return;
-  const int n_kv = max(n0, n1);
-  const int q0 = p.cu_q_lens[s];
-  const int n_pages = (L + p.bs - 1) / p.bs;
+  const int units = *p.item_count * p.G;
+  if ((int)blockIdx.x >= units) return;
 
   if (threadIdx.x == 0) {
     // full barriers: one arrival per producer warp of the ring; p_full: 128 softmax threads
-    for (int i = 0; i < 18; ++i) mbar_init(&bars[i], (i == 13 || i == 14) ? 128 : ((i >= 1 && i <= 3) || (i >= 7 && i <= 8)) ? 2 : 1);
+    for (int i = 0; i < 23; ++i)
+      mbar_init(&bars[i], (i == 13 || i == 14) ? 128
+                          : ((i >= 1 && i <= 3) || (i >= 7 && i <= 8)) ? 2
+                          : (i >= 21) ? kUnitReaders : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -255,29 +290,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   };
   // every role calls waits with all 32 lanes: agree on the outcome before any warp-collective op
   auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(bar, parity)); };
+  // The k-th unit of this CTA, from the unit ring: 1 = a unit, 0 = no more, -1 = aborted.
+  auto next_unit = [&](uint32_t& k, PfUnit& it, bool flag) -> int {
+    const int slot = k & 1;
+    if (!wait_all(&unit_full[slot], (k >> 1) & 1)) return -1;
+    const int u = unit_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&unit_empty[slot]);
+    ++k;
+    if (u < 0) return 0;
+    pf_unit(p, u, flag, it);
+    return 1;
+  };
 
+  // Ring positions run on across units: K/V tile t (counted over every unit this
+  // CTA has processed) sits in K stage t % kKStages and V stage t % 2, and each
+  // barrier's phase is the number of its earlier completions.
   if (warp >= 8 && warp < kMmaWarp) {
-    // ------------------------------------------------------------ TMA producers
-    regs_dec<kRegsLow>();
+    // ------------------------------------------------------------ K/V producers
+    regs_dec<kRegsProd>();
     const int pw = warp - 8;
     const bool is_k = pw < 2;
     const int part = pw & 1;                   // which half of each tile's pages
-    const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
-    if (pw == 0 && lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int ntiles = n1 > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * Sh::kQBytes));
-      const uint64_t pol = l2_policy_evict_first();
-      for (int w = 0; w < ntiles; ++w) {
-        const int qi0 = (2 * pair + w) * p.Tq;
-        for (int hh = 0; hh < p.r; ++hh)
-          for (int h = 0; h < HALVES; ++h)
-            tma_load_3d(sQ + w * Sh::kQBytes + h * Sh::kQHalf + hh * p.Tq * 128, &tmQ, q_full, h * 64, g * p.r + hh,
-                        q0 + qi0, pol);
-      }
-    }
     const CUtensorMap* map = is_k ? &tmK : &tmV;
     uint8_t* ring = is_k ? sK : sV;
     uint64_t* full = is_k ? k_full : v_full;
@@ -286,40 +320,50 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     const int half_pg = npg >> 1;              // pages of this warp
     const uint64_t pol = l2_policy_evict_last();
     const int depth = is_k ? kKStages : 2;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % depth;
-      const int lp = part * half_pg + lane;    // page index inside the tile
-      const int pg = j * npg + lp;
-      const bool live = lane < half_pg && pg < n_pages;
-      int rowc = 0;
-      if (live) {
-        const int b = checked_block(bt_row, pg, p.num_blocks, &g_status_prefill);
-        rowc = b < 0 ? -p.bs : b * p.bs;   // a bad id reads a box entirely out of bounds: zeros
+    if (lane == 0) tma_prefetch_desc(map);
+    uint32_t t = 0, k = 0;                     // tiles issued so far, units read
+    bool ok = true;
+    PfUnit it;
+    while (ok && next_unit(k, it, false) > 0) {
+      const int32_t* bt_row = p.block_table + (size_t)it.s * p.max_blocks;
+      for (int j = 0; j < it.n_kv; ++j, ++t) {
+        const int st = t % depth;
+        const int lp = part * half_pg + lane;  // page index inside the tile
+        const int pg = j * npg + lp;
+        const bool live = lane < half_pg && pg < it.n_pages;
+        int rowc = 0;
+        if (live) {
+          const int b = checked_block(bt_row, pg, p.num_blocks, &g_status_prefill);
+          rowc = b < 0 ? -p.bs : b * p.bs;   // a bad id reads a box entirely out of bounds: zeros
+        }
+        const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, live)) * p.bs * 128 * HALVES;
+        if (t >= (uint32_t)depth && !wait_all(&empty[st], ((t / depth) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+        __syncwarp();
+        if (live)
+          for (int h = 0; h < HALVES; ++h)
+            tma_load_3d(ring + st * Sh::kKvBytes + h * Sh::kKvHalf + lp * p.bs * 128, map, &full[st], h * 64, it.g,
+                        rowc, pol);
       }
-      const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, live)) * p.bs * 128 * HALVES;
-      if (j >= depth && !wait_all(&empty[st], ((j / depth) - 1) & 1)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
-      __syncwarp();
-      if (live)
-        for (int h = 0; h < HALVES; ++h)
-          tma_load_3d(ring + st * Sh::kKvBytes + h * Sh::kKvHalf + lp * p.bs * 128, map, &full[st], h * 64, g, rowc,
-                      pol);
     }
     if (*abort_flag) {
       // let the loads still in flight land before the CTA's memory goes away
-      for (int j = max(0, n_kv - depth); j < n_kv; ++j) mbar_wait(&full[j % depth], (j / depth) & 1, &g_status_prefill);
+      for (uint32_t k = t > (uint32_t)depth ? t - depth : 0; k < t; ++k)
+        mbar_wait(&full[k % depth], (k / depth) & 1, &g_status_prefill);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ UMMA issuer
-    regs_dec<kRegsLow>();
+    regs_dec<kRegsMma>();
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kRows, kKvTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kRows, D, false, true);
-    const int nw[2] = {n0, n1};
     bool issued = false;
-    auto qk = [&](int w, int j) {  // S_w = Q_w K_j^T
+    auto qk = [&](int w, uint32_t t) {  // S_w = Q_w K_t^T
       if (lane == 0) {
         const uint32_t qbase = smem_u32(sQ + w * Sh::kQBytes);
-        const uint32_t kbase = smem_u32(sK + (j % kKStages) * Sh::kKvBytes);
+        const uint32_t kbase = smem_u32(sK + (t % kKStages) * Sh::kKvBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t within = (kk & 3) * 32;
@@ -329,75 +373,98 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         umma_commit(&s_full[w]);
       }
     };
-    auto pv = [&](int w, int j) {  // O_w += P_w V_j, P_w from the first 64 columns of S_w
+    auto pv = [&](int w, uint32_t t, bool first) {  // O_w (+)= P_w V_t, P_w from the first 64 columns of S_w
       if (lane == 0) {
-        const uint32_t vbase = smem_u32(sV + (j & 1) * Sh::kKvBytes);
+        const uint32_t vbase = smem_u32(sV + (t & 1) * Sh::kKvBytes);
         const uint32_t o_tmem = tmem + 2 * kKvTile + w * D;
 #pragma unroll
         for (int kk = 0; kk < kKvTile / 16; ++kk)
           umma_bf16_tmem_a(o_tmem, tmem + w * kKvTile + kk * 8,
-                           umma_desc_sw128(vbase + kk * 2048, Sh::kKvHalf, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+                           umma_desc_sw128(vbase + kk * 2048, Sh::kKvHalf, 1024), kIdPV, (!first || kk > 0) ? 1u : 0u);
         umma_commit(&pv_done[w]);
       }
     };
-    bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
-    if (ok) {
-      tc_fence_after_sync();
-      qk(0, 0);
-      if (n1 > 0) qk(1, 0);
-      if (lane == 0) umma_commit(&k_empty[0]);  // stage of tile 0
-      issued = true;
-      __syncwarp();
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int vst = j & 1;
-      if (!wait_all(&v_full[vst], (j >> 1) & 1)) {
+    uint32_t t_base = 0, n_units = 0, np[2] = {0u, 0u};  // tiles, units, p_full phases consumed
+    uint32_t k = 0;
+    bool ok = true;
+    PfUnit it;
+    while (ok) {
+      const int r = next_unit(k, it, false);
+      if (r <= 0) {
+        ok = r == 0;
+        break;
+      }
+      const int nw[2] = {it.n0, it.n1};
+      if (!wait_all(q_full, n_units & 1) || !wait_all(&k_full[t_base % kKStages], (t_base / kKStages) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int tok0 = j * kKvTile;
-      if (tok0 + kKvTile > L) {
-        // rows past the sequence end may hold anything (NaN included): zero them so that P = 0 stays 0
-        uint8_t* vb = sV + vst * Sh::kKvBytes;
-        for (int row = (L - tok0) + lane; row < kKvTile; row += 32)
-          for (int h = 0; h < HALVES; ++h) {
-            uint4* d = reinterpret_cast<uint4*>(vb + h * Sh::kKvHalf + row * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        fence_proxy_async_smem();
-        __syncwarp();
+      qk(0, t_base);
+      if (it.n1 > 0) qk(1, t_base);
+      if (lane == 0) {
+        umma_commit(&k_empty[t_base % kKStages]);
+        if (it.n_kv == 1) umma_commit(q_free);  // the unit's last QK is issued
       }
-      const bool more = j + 1 < n_kv;
-      bool k_ready = false;
-      for (int w = 0; w < 2; ++w) {
-        if (j < nw[w]) {
-          if (!wait_all(&p_full[w], j & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          pv(w, j);
-          // the V stage is free once the last PV of this tile has run
-          if (lane == 0 && (w == 1 || nw[1] <= j)) umma_commit(&v_empty[vst]);
+      issued = true;
+      __syncwarp();
+      for (int j = 0; ok && j < it.n_kv; ++j) {
+        const uint32_t t = t_base + j;
+        const int vst = t & 1;
+        if (!wait_all(&v_full[vst], (t >> 1) & 1)) {
+          ok = false;
+          break;
         }
-        if (more && j + 1 < nw[w]) {
-          if (!k_ready) {  // K_{j+1} is waited for only after PV0_j is on its way
-            if (!wait_all(&k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1)) {
+        tc_fence_after_sync();
+        const int tok0 = j * kKvTile;
+        if (tok0 + kKvTile > it.L) {
+          // rows past the sequence end may hold anything (NaN included): zero them so that P = 0 stays 0
+          uint8_t* vb = sV + vst * Sh::kKvBytes;
+          for (int row = (it.L - tok0) + lane; row < kKvTile; row += 32)
+            for (int h = 0; h < HALVES; ++h) {
+              uint4* d = reinterpret_cast<uint4*>(vb + h * Sh::kKvHalf + row * 128);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        const bool more = j + 1 < it.n_kv;
+        bool k_ready = false;
+        for (int w = 0; w < 2; ++w) {
+          if (j < nw[w]) {
+            if (!wait_all(&p_full[w], np[w] & 1)) {
               ok = false;
               break;
             }
+            ++np[w];
             tc_fence_after_sync();
-            k_ready = true;
+            pv(w, t, j == 0);
+            // the V stage is free once the last PV of this tile has run
+            if (lane == 0 && (w == 1 || nw[1] <= j)) umma_commit(&v_empty[vst]);
           }
-          qk(w, j + 1);
+          if (more && j + 1 < nw[w]) {
+            if (!k_ready) {  // K_{t+1} is waited for only after PV0_t is on its way
+              if (!wait_all(&k_full[(t + 1) % kKStages], ((t + 1) / kKStages) & 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              k_ready = true;
+            }
+            qk(w, t + 1);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0 && more) {
+          umma_commit(&k_empty[(t + 1) % kKStages]);
+          if (j + 2 == it.n_kv) umma_commit(q_free);  // the unit's last QK is issued
         }
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0 && more) umma_commit(&k_empty[(j + 1) % kKStages]);
-      __syncwarp();
+      t_base += it.n_kv;
+      ++n_units;
     }
     if (!ok && issued) {
       // wait (bounded) for every UMMA this warp issued before TMEM is freed
@@ -405,21 +472,64 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       __syncwarp();
       mbar_wait(drain, 0, &g_status_prefill);
     }
+  } else if (warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------ query loader
+    regs_dec<kRegsMma>();
+    if (lane == 0) tma_prefetch_desc(&tmQ);
+    uint32_t n_units = 0, k = 0;
+    PfUnit it;
+    while (next_unit(k, it, false) > 0) {
+      // the previous unit's query tiles stay until its last QK has completed
+      if (n_units > 0 && !wait_all(q_free, (n_units - 1) & 1)) break;
+      if (lane == 0) {
+        const int ntiles = it.n1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * Sh::kQBytes));
+        const uint64_t pol = l2_policy_evict_first();
+        for (int w = 0; w < ntiles; ++w) {
+          const int qi0 = (2 * it.pair + w) * p.Tq;
+          for (int hh = 0; hh < p.r; ++hh)
+            for (int h = 0; h < HALVES; ++h)
+              tma_load_3d(sQ + w * Sh::kQBytes + h * Sh::kQHalf + hh * p.Tq * 128, &tmQ, q_full, h * 64,
+                          it.g * p.r + hh, it.q0 + qi0, pol);
+        }
+      }
+      __syncwarp();
+      ++n_units;
+    }
+    if (*abort_flag && n_units > 0) mbar_wait(q_full, (n_units - 1) & 1, &g_status_prefill);
+  } else if (warp == kMmaWarp + 2) {
+    // ------------------------------------------------------------ unit fetcher
+    // claims units from the global list, heaviest first, and publishes them to
+    // the other warps through the two-slot unit ring; -1 ends the walk
+    regs_dec<kRegsMma>();
+    uint32_t k = 0;
+    for (;;) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(p.unit_head, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u < units) {
+        PfUnit it;
+        if (!pf_unit(p, u, lane == 0, it)) continue;   // nothing to compute (length errors flagged here)
+      } else {
+        u = -1;
+      }
+      const int slot = k & 1;
+      if (k >= 2 && !wait_all(&unit_empty[slot], ((k >> 1) - 1) & 1)) break;
+      if (lane == 0) {
+        unit_slot[slot] = u;
+        mbar_arrive(&unit_full[slot]);
+      }
+      __syncwarp();
+      ++k;
+      if (u < 0) break;
+    }
   } else if (warp > kMmaWarp) {
-    regs_dec<kRegsLow>();  // idle: give the registers to the softmax groups
+    regs_dec<kRegsMma>();  // idle: give the registers to the softmax groups
   } else {
     // ------------------------------------------------------------ softmax groups
     regs_inc<kRegsSoftmax>();
     const int w = warp >> 2;                    // query tile of this group
-    const int nkv = w ? n1 : n0;
     const int row = (warp & 3) * 32 + lane;
-    const int hh = row / p.Tq;
-    const int qi0 = (2 * pair + w) * p.Tq;
-    const int qi = qi0 + (row - hh * p.Tq);
-    const bool row_valid = nkv > 0 && qi < q_len;
-    const int p_min = L - q_len + qi0;          // position of the tile's first query token
-    const int p_max = L - q_len + min(q_len - 1, qi0 + p.Tq - 1);
-    const int p_row = row_valid ? (L - q_len + qi) : p_max;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_tmem = lane_base + w * kKvTile;
     const uint32_t o_tmem = lane_base + 2 * kKvTile + w * D;
@@ -428,96 +538,115 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     // |sl2| > 0 keeps -inf (hidden key) * |sl2| = -inf; a zero scale becomes 1e-30, which
     // leaves every exponent equal to the max to fp32 precision (uniform weights)
     const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
-    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t ns = 0, npv = 0, k = 0;            // s_full phases consumed, PVs of this group, units read
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!wait_all(&s_full[w], j & 1)) {
+    PfUnit it;
+    while (ok && next_unit(k, it, false) > 0) {
+      const int nkv = w ? it.n1 : it.n0;
+      if (nkv == 0) continue;                   // no second query tile in this unit
+      const int L = it.L, q_len = it.q_len;
+      const int hh = row / p.Tq;
+      const int qi0 = (2 * it.pair + w) * p.Tq;
+      const int qi = qi0 + (row - hh * p.Tq);
+      const bool row_valid = qi < q_len;
+      const int p_min = L - q_len + qi0;        // position of the tile's first query token
+      const int p_max = L - q_len + min(q_len - 1, qi0 + p.Tq - 1);
+      const int p_row = row_valid ? (L - q_len + qi) : p_max;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        if (!wait_all(&s_full[w], ns & 1)) {
+          ok = false;
+          break;
+        }
+        ++ns;
+        tc_fence_after_sync();
+        const int tok0 = j * kKvTile;
+        // Visible keys of this row in this tile form a prefix: t <= p_row.
+        const int vis = tok0 + kKvTile - 1 > p_min ? min(max(p_row - tok0 + 1, 0), kKvTile) : kKvTile;
+        const bool lean = vis == kKvTile && sgn > 0.f;   // the common case: no mask, positive scale
+        // the row's 128 scores, read once
+        uint32_t sv[kKvTile];
+#pragma unroll
+        for (int c = 0; c < kKvTile; c += 32) tmem_ld32(s_tmem + c, sv + c);
+        tmem_ld_wait();
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        if (lean) {
+#pragma unroll
+          for (int c = 0; c < kKvTile; c += 2)
+            mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKvTile; ++c)
+            mx[c & 7] = fmaxf(mx[c & 7], c < vis ? __uint_as_float(sv[c]) * sgn : -INFINITY);
+        }
+        const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
+        const bool grow = m_new > m_run + 8.0f;   // rescale only when the max grew past 2^8
+        float alpha = 1.f;
+        if (grow) {
+          alpha = exp2_approx(m_run - m_new);
+          m_run = m_new;
+        }
+        if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+          // PV_w_{j-1} has completed: it was issued before QK_w_j, whose result we hold
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_tmem + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(o_tmem + c * 32, ov);
+          }
+        }
+        l_run *= alpha;
+        // P = exp2(s * |sl2| - m) as bf16 pairs (even token in the low half), packed in
+        // place into sv[0, 64) and stored over the first 64 columns of S_w
+        const float neg_m = -m_run;
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // row sums, as packed pairs
+        const uint64_t asl2_2 = f2_pack(asl2, asl2), neg_m2 = f2_pack(neg_m, neg_m);
+        if (lean) {
+          // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
+#pragma unroll
+          for (int c = 0; c < kKvTile; c += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
+            const float e0 = exp2_approx(x0);
+            const float e1 = exp2_approx(x1);
+            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
+            sv[c >> 1] = pack_bf16x2(e0, e1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKvTile; c += 2) {
+            const float e0 = c < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
+            const float e1 = c + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
+            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
+            sv[c >> 1] = pack_bf16x2(e0, e1);
+          }
+        }
+        tmem_st32(s_tmem, sv);
+        tmem_st32(s_tmem + 32, sv + 32);
+        float ls[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f2_unpack(ls2[i], ls[2 * i], ls[2 * i + 1]);
+        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&p_full[w]);
+      }
+      if (!ok) break;
+      npv += nkv;
+      if (!wait_all(&pv_done[w], (npv - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int tok0 = j * kKvTile;
-      // Visible keys of this row in this tile form a prefix: t <= p_row.
-      const int vis = tok0 + kKvTile - 1 > p_min ? min(max(p_row - tok0 + 1, 0), kKvTile) : kKvTile;
-      const bool lean = vis == kKvTile && sgn > 0.f;   // the common case: no mask, positive scale
-      // the row's 128 scores, read once
-      uint32_t sv[kKvTile];
-#pragma unroll
-      for (int c = 0; c < kKvTile; c += 32) tmem_ld32(s_tmem + c, sv + c);
-      tmem_ld_wait();
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-      if (lean) {
-#pragma unroll
-        for (int c = 0; c < kKvTile; c += 2)
-          mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKvTile; ++c)
-          mx[c & 7] = fmaxf(mx[c & 7], c < vis ? __uint_as_float(sv[c]) * sgn : -INFINITY);
-      }
-      const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
-      const bool grow = m_new > m_run + 8.0f;   // rescale only when the max grew past 2^8
-      float alpha = 1.f;
-      if (grow) {
-        alpha = exp2_approx(m_run - m_new);
-        m_run = m_new;
-      }
-      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-        // PV_w_{j-1} has completed: it was issued before QK_w_j, whose result we hold
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(o_tmem + c * 32, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(o_tmem + c * 32, ov);
-        }
-      }
-      l_run *= alpha;
-      // P = exp2(s * |sl2| - m) as bf16 pairs (even token in the low half), packed in
-      // place into sv[0, 64) and stored over the first 64 columns of S_w
-      const float neg_m = -m_run;
-      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // row sums, as packed pairs
-      const uint64_t asl2_2 = f2_pack(asl2, asl2), neg_m2 = f2_pack(neg_m, neg_m);
-      if (lean) {
-        // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
-#pragma unroll
-        for (int c = 0; c < kKvTile; c += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
-          const float e0 = exp2_approx(x0);
-          const float e1 = exp2_approx(x1);
-          ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
-          sv[c >> 1] = pack_bf16x2(e0, e1);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKvTile; c += 2) {
-          const float e0 = c < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
-          const float e1 = c + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
-          ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
-          sv[c >> 1] = pack_bf16x2(e0, e1);
-        }
-      }
-      tmem_st32(s_tmem, sv);
-      tmem_st32(s_tmem + 32, sv + 32);
-      float ls[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) f2_unpack(ls2[i], ls[2 * i], ls[2 * i + 1]);
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&p_full[w]);
-    }
-    if (nkv > 0 && ok && wait_all(&pv_done[w], (nkv - 1) & 1)) {
-      tc_fence_after_sync();
       const float inv = 1.0f / l_run;
-      const int head = g * p.r + hh;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(q0 + qi) * p.H + head) * D;
+      const int head = it.g * p.r + hh;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(it.q0 + qi) * p.H + head) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -535,7 +664,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
           }
         }
       }
-      if (row_valid && p.lse_out) p.lse_out[(size_t)(q0 + qi) * p.H + head] = (m_run + log2f(l_run)) * kLn2;
+      if (row_valid && p.lse_out) p.lse_out[(size_t)(it.q0 + qi) * p.H + head] = (m_run + log2f(l_run)) * kLn2;
+      // the next unit's first PV_w overwrites O_w: every lane has read it
+      tc_fence_before_sync();
     }
   }
 
@@ -576,6 +707,7 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
   int4* items = reinterpret_cast<int4*>(reinterpret_cast<char*>(workspace) + 256);
   p.items = items;
   p.item_count = count;
+  p.unit_head = count + 1;
   CUtensorMap tmQ, tmK, tmV;
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)p.H, (uint64_t)p.T};
   const uint64_t qstr[2] = {(uint64_t)D * 2, (uint64_t)p.H * D * 2};
@@ -609,8 +741,14 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
                   kRegsLaunch);
     regs_checked = 1;
   }
-  return launch_dependent(kern, dim3((unsigned)(max_items * p.G)), dim3(kPfThreads), smem, st,
-                          "prefill_bf16_kernel launch", tmQ, tmK, tmV, p);
+  // persistent: at most one CTA per SM, each taking units from the list as it goes
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(METIS_E_CUDA, "querying the SM count: %s", cudaGetErrorString(e));
+  const size_t grid = std::min<size_t>(max_items * p.G, (size_t)std::max(sms, 1));
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(kPfThreads), smem, st, "prefill_bf16_kernel launch", tmQ,
+                          tmK, tmV, p);
 }
 
 }  // namespace metis

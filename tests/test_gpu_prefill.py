@@ -43,7 +43,10 @@ def check(case):
 
 @pytest.mark.parametrize("prefix,q_len", [(0, 1), (0, 5), (0, 32), (0, 33), (0, 128), (0, 129), (1, 31),
                                           (15, 64), (16, 100), (17, 512), (127, 1), (128, 200), (300, 77),
-                                          (1000, 256)])
+                                          (1000, 256),
+                                          # one query tile over 2, 3 and 40 K/V tiles, a causal mask inside
+                                          # the second tile, lengths at the tile edge
+                                          (130, 1), (254, 1), (255, 1), (257, 3), (200, 30), (5000, 20)])
 def test_single_sequence(prefix, q_len):
     case = wl.make_prefill_case(100 + prefix + q_len, [prefix], [q_len], H=32, G=8, D=128, bs=16,
                                 dtype=torch.bfloat16, extra_blocks=3, poison=True)
