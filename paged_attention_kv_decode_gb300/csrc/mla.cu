@@ -75,12 +75,21 @@ constexpr int kMlaUnit = 32;        // tokens per exchange / softmax / P V unit 
 constexpr int kMlaTile = 64;        // tokens per score UMMA (two units)
 constexpr int kMlaRows = 128;       // heads per head tile (the UMMA M)
 constexpr int kMlaOwn = 64;         // heads whose softmax a CTA runs
-constexpr int kMlaThreads = 384;    // 12 warps
+constexpr int kMlaThreads = 512;    // 16 warps
+constexpr int kMlaRegsRow = 160;    // warpgroups 0 and 3: the two row-warp sets
+constexpr int kMlaRegsLow = 96;     // warpgroups 1 and 2: staging/rescale, TMA, UMMA, exchanges
+static_assert(128 * (2 * kMlaRegsRow + 2 * kMlaRegsLow) <= 65536, "register split exceeds the register file");
 constexpr int kMlaTmemCols = 512;
 constexpr int kMlaSortMax = 2048;
-constexpr int kMlaStages = 8;       // ring stages of one unit (even: a tile is two adjacent stages)
-constexpr int kMlaNX = 2;           // partial-score exchange slots
-constexpr int kMlaNP = 3;           // P tile slots
+#ifndef METIS_MLA_STAGES
+#define METIS_MLA_STAGES 8
+#define METIS_MLA_NX 2
+#define METIS_MLA_NP 3
+#endif
+constexpr int kMlaStages = METIS_MLA_STAGES;  // ring stages of one unit (even: a tile is two adjacent stages)
+constexpr int kMlaNX = METIS_MLA_NX;          // partial-score exchange slots (even: each row set uses every other)
+constexpr int kMlaNP = METIS_MLA_NP;          // P tile slots
+static_assert(kMlaStages % 2 == 0 && kMlaNX % 2 == 0, "stage and exchange-slot counts must be even");
 constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
 constexpr uint32_t kTmS = 256;      // 2 x 64 columns: partial scores of a tile
 constexpr uint32_t kTmQ = 384;      // 128 columns: latent part of Q_r as bf16 pairs
@@ -98,9 +107,32 @@ struct MlaShape {
   static constexpr int kP = kRx + kMlaNX * kXBuf;         // kMlaNP P tiles
   static constexpr int kAlpha = kP + kMlaNP * kPBuf;      // kMlaNP x 128 rescale factors (head order)
   static constexpr int kStat = kAlpha + kMlaNP * kMlaRows * 4;  // 128 x {m, l} (head order)
-  static constexpr int kBars = kStat + kMlaRows * 8;
-  static constexpr int kSmem = kBars + 512 + 1024;        // + alignment slack
+  static constexpr int kHand = kStat + kMlaRows * 8;       // 2 sets x 128 running maxima + 128 row-sum shares
+  static constexpr int kBars = kHand + 3 * kMlaRows * 4;
+  static constexpr int kSmem = kBars + 1024 + 1024;       // barriers + alignment slack
 };
+static_assert(MlaShape::kSmem <= 227 * 1024, "MLA shared memory exceeds the per-CTA limit");
+
+// mbarrier layout (indices into the barrier area) and arrival counts
+struct MlaBar {
+  static constexpr int kKvFull = 0, kKvEmpty = kKvFull + kMlaStages, kSFull = kKvEmpty + kMlaStages,
+                       kPvDone = kSFull + 2, kStaged = kPvDone + 4, kRxFull = kStaged + kMlaNX,
+                       kRxRead = kRxFull + kMlaNX, kTxOk = kRxRead + kMlaNX, kPLocal = kTxOk + kMlaNX,
+                       kPRemote = kPLocal + kMlaNP, kPRelay = kPRemote + kMlaNP, kPslotOk = kPRelay + kMlaNP,
+                       kQFull = kPslotOk + kMlaNP, kStatLocal = kQFull + 1, kStatFull = kStatLocal + 1,
+                       kDrain = kStatFull + 1, kSFree = kDrain + 1, kHand = kSFree + 2, kFin = kHand + 8,
+                       kCount = kFin + 1;
+  __host__ __device__ static constexpr int arrivals(int i) {
+    return (i >= kSFree && i < kSFree + 2) ? 256
+           : (i >= kHand && i < kHand + 8) ? 32
+           : ((i >= kStaged && i < kStaged + kMlaNX) || (i >= kRxRead && i < kRxRead + kMlaNX) ||
+              (i >= kPLocal && i < kPLocal + kMlaNP) || (i >= kPRelay && i < kPRelay + kMlaNP) || i == kQFull ||
+              i == kStatLocal || i == kFin)
+               ? 128
+               : 1;
+  }
+};
+static_assert((MlaBar::kCount + 2) * 8 <= 1024, "MLA barrier area");
 
 struct MlaParams {
   const uint4* q;   // [S, H, 576] bf16, read as 16-byte chunks
@@ -191,25 +223,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   float* sAlpha = reinterpret_cast<float*>(smem + Sh::kAlpha);
   float* sStat = reinterpret_cast<float*>(smem + Sh::kStat);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBars);
-  uint64_t* kv_full = bars + 0;     // [kMlaStages]
-  uint64_t* kv_empty = bars + 8;    // [kMlaStages]
-  uint64_t* s_full = bars + 16;     // [2] partial scores of tile j in S[j & 1]
-  uint64_t* pv_done = bars + 18;    // [4] P V of unit u completed, on u % 4
-  uint64_t* staged = bars + 22;     // [kMlaNX] partial scores of the peer's heads staged (128 arrivals)
-  uint64_t* rx_full = bars + 24;    // [kMlaNX] the peer's partial of own heads landed (armed with expect_tx)
-  uint64_t* rx_read = bars + 26;    // [kMlaNX] a receive buffer has been read (128 arrivals)
-  uint64_t* tx_ok = bars + 28;      // [kMlaNX] credit from the peer: it has read what we sent (remote)
-  uint64_t* p_local = bars + 30;    // [kMlaNP] P of own heads + factors written (128 arrivals)
-  uint64_t* p_remote = bars + 33;   // [kMlaNP] P of the peer's heads + factors landed (armed with expect_tx)
-  uint64_t* p_relay = bars + 36;    // [kMlaNP] O rescaled for the unit, P complete (128 arrivals)
-  uint64_t* pslot_ok = bars + 39;   // [kMlaNP] credit from the peer: its P slot is free (remote)
-  uint64_t* q_full = bars + 42;     // Q_r in TMEM / shared memory (128 arrivals)
-  uint64_t* stat_local = bars + 43; // final statistics of own heads written (128 arrivals)
-  uint64_t* stat_full = bars + 44;  // final statistics of the peer's heads landed (armed with expect_tx)
-  uint64_t* drain = bars + 45;
-  uint64_t* s_free = bars + 46;     // [2] the row warps have read S[j & 1] of tile j (128 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 48);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 49);
+  uint64_t* kv_full = bars + MlaBar::kKvFull;       // [kMlaStages]
+  uint64_t* kv_empty = bars + MlaBar::kKvEmpty;     // [kMlaStages]
+  uint64_t* s_full = bars + MlaBar::kSFull;         // [2] partial scores of tile j in S[j & 1]
+  uint64_t* pv_done = bars + MlaBar::kPvDone;       // [4] P V of unit u completed, on u % 4
+  uint64_t* staged = bars + MlaBar::kStaged;        // [kMlaNX] partial scores of the peer's heads staged (128 arrivals)
+  uint64_t* rx_full = bars + MlaBar::kRxFull;       // [kMlaNX] the peer's partial of own heads landed (armed with expect_tx)
+  uint64_t* rx_read = bars + MlaBar::kRxRead;       // [kMlaNX] a receive buffer has been read (128 arrivals)
+  uint64_t* tx_ok = bars + MlaBar::kTxOk;           // [kMlaNX] credit from the peer: it has read what we sent (remote)
+  uint64_t* p_local = bars + MlaBar::kPLocal;       // [kMlaNP] P of own heads + factors written (128 arrivals)
+  uint64_t* p_remote = bars + MlaBar::kPRemote;     // [kMlaNP] P of the peer's heads + factors landed (armed with expect_tx)
+  uint64_t* p_relay = bars + MlaBar::kPRelay;       // [kMlaNP] O rescaled for the unit, P complete (128 arrivals)
+  uint64_t* pslot_ok = bars + MlaBar::kPslotOk;     // [kMlaNP] credit from the peer: its P slot is free (remote)
+  uint64_t* q_full = bars + MlaBar::kQFull;         // Q_r in TMEM / shared memory (128 arrivals)
+  uint64_t* stat_local = bars + MlaBar::kStatLocal; // final statistics of own heads written (128 arrivals)
+  uint64_t* stat_full = bars + MlaBar::kStatFull;   // final statistics of the peer's heads landed (armed with expect_tx)
+  uint64_t* drain = bars + MlaBar::kDrain;
+  uint64_t* s_free = bars + MlaBar::kSFree;         // [2] both units of tile j have been read from S[j & 1] (256 arrivals)
+  uint64_t* hand = bars + MlaBar::kHand;            // [2 sets][4 quarters] running max after a unit of that set (32 arrivals)
+  uint64_t* fin = bars + MlaBar::kFin;              // set 1's share of the row sums handed to set 0 (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + MlaBar::kCount);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + MlaBar::kCount + 1);
+  float* sHand = reinterpret_cast<float*>(smem + Sh::kHand);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
@@ -253,11 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   constexpr uint32_t kPHalfBytes = kMlaOwn * 64 + kMlaOwn * 4;  // P rows + factors of 64 heads
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 48; ++i) {
-      const bool many = (i >= 22 && i <= 23) || (i >= 26 && i <= 27) || (i >= 30 && i <= 32) || (i >= 36 && i <= 38) ||
-                        i == 42 || i == 43 || i == 46 || i == 47;
-      mbar_init(&bars[i], many ? 128 : 1);
-    }
+    for (int i = 0; i < MlaBar::kCount; ++i) mbar_init(&bars[i], MlaBar::arrivals(i));
     *abort_flag = 0;
     fence_barrier_init();
     // arm the receive slots for the first units and the final statistics
@@ -294,6 +325,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    regs_dec<kMlaRegsLow>();
     // Per unit and page piece: lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3,
     // lane 5 pi + 4 the rope half block 512 + 32 r .. + 31.
     const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
@@ -335,6 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         mbar_wait(&kv_full[u % kMlaStages], (u / kMlaStages) & 1, &g_status_mla);
   } else if (warp == 9) {
     // ------------------------------------------------------------ UMMA issuer
+    regs_dec<kMlaRegsLow>();
     constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kMlaRows, kMlaTile, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kMlaRows, kMlaHalf, false, true);
     const uint32_t kv = smem_u32(sKV), rope = smem_u32(sRope), qr = smem_u32(sQr), pt = smem_u32(sP);
@@ -423,10 +456,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ score exchange
+    regs_dec<kMlaRegsLow>();
     const uint32_t peer_rx = dsmem_map(smem_u32(sRx), peer);
     const uint32_t peer_rx_full = dsmem_map(smem_u32(rx_full), peer);
     const uint32_t peer_tx_ok = dsmem_map(smem_u32(tx_ok), peer);
-    int armed0 = 0, armed1 = n_units > 1 ? 1 : -1;
+    int armed[kMlaNX];
+#pragma unroll
+    for (int x = 0; x < kMlaNX; ++x) armed[x] = x < n_units ? x : -1;
     for (int t = 0; t <= n_units; ++t) {
       if (t < n_units) {  // staged unit t -> the peer's receive slot t % kMlaNX
         const int x = t % kMlaNX;
@@ -445,18 +481,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           mbar_arrive_expect_tx(&rx_full[x], Sh::kXBuf);
           mbar_arrive_remote_relaxed(peer_tx_ok + x * 8);
         }
-        if (x) armed1 = u + kMlaNX;
-        else armed0 = u + kMlaNX;
+#pragma unroll
+        for (int y = 0; y < kMlaNX; ++y)
+          if (y == x) armed[y] = u + kMlaNX;
         __syncwarp();
       }
     }
     // after an abort, let the peer's copies already on their way land before this CTA exits
     if (lane == 0 && *abort_flag) {
-      if (armed0 >= 0) mbar_wait(&rx_full[0], (armed0 / kMlaNX) & 1, &g_status_mla);
-      if (armed1 >= 0) mbar_wait(&rx_full[1], (armed1 / kMlaNX) & 1, &g_status_mla);
+#pragma unroll
+      for (int x = 0; x < kMlaNX; ++x)
+        if (armed[x] >= 0) mbar_wait(&rx_full[x], (armed[x] / kMlaNX) & 1, &g_status_mla);
     }
   } else if (warp == 11) {
     // ------------------------------------------------------------ P exchange
+    regs_dec<kMlaRegsLow>();
     const uint32_t peer_p = dsmem_map(smem_u32(sP), peer);
     const uint32_t peer_alpha = dsmem_map(smem_u32(sAlpha), peer);
     const uint32_t peer_p_remote = dsmem_map(smem_u32(p_remote), peer);
@@ -511,8 +550,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         if (armed[x] >= 0) mbar_wait(&p_remote[x], (armed[x] / kMlaNP) & 1, &g_status_mla);
       mbar_wait(stat_full, 0, &g_status_mla);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ rescale warps
+    regs_dec<kMlaRegsLow>();
     const int quarter = warp - 4;
     const int hh = 64 * (lane >> 4) + 16 * quarter + (lane & 15);  // head (in the tile) of this lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -547,7 +587,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ row warps
-    const int quarter = warp;
+    // Two sets over the same lanes: warps 0-3 take the even units, warps 12-15 the
+    // odd ones; the running max passes from set to set after every unit.
+    regs_inc<kMlaRegsRow>();
+    const int set = warp >> 3;
+    const int quarter = warp & 3;
     const int g = lane >> 4, li = lane & 15;
     const bool own = g == (int)rank;
     const int xi = 16 * quarter + li;               // row within a 64-head half
@@ -557,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const int prow = 32 * quarter + 16 * (int)rank + li;  // P row / TMEM lane of the own head this lane works on
     const int tok_half = own ? 0 : 16;                // tokens of a unit this lane exponentiates
-    {
+    if (set == 0) {
       // Q_r of this lane's head: latent dims 256 r .. 256 r + 255 into TMEM columns
       // kTmQ.. as bf16 pairs (the raw row words), rope dims 512 + 32 r .. + 31 into
       // row `lane` of the 64-byte-swizzled shared tile (chunk c at c ^ ((row >> 1) & 3)).
@@ -587,16 +631,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
     auto load_s = [&](int u, uint32_t* v) -> bool {  // this CTA's partial scores of unit u, every lane
       const int j = u >> 1;
-      if ((u & 1) == 0) {
-        if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) return false;
-        tc_fence_after_sync();
-      }
+      if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) return false;
+      tc_fence_after_sync();
       tmem_ld32(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * kMlaUnit, v);
       tmem_ld_wait();
-      if ((u & 1) == 1 || u + 1 == n_units) {  // last read of S[j & 1] for tile j
-        tc_fence_before_sync();
-        mbar_arrive(&s_free[j & 1]);
-      }
+      tc_fence_before_sync();
+      mbar_arrive(&s_free[j & 1]);  // each unit of a tile is read once, by the set that owns it
       return true;
     };
     auto stage = [&](int u, const uint32_t* v) -> bool {  // the peer's heads of unit u -> staging slot
@@ -612,14 +652,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       mbar_arrive(&staged[x]);
       return true;
     };
+    // The running max after unit v (processed by the other set): take it, and bring
+    // this set's share of the row sum, kept relative to the max it last saw, up to date.
+    auto catch_up = [&](int v, float& m_run, float& l_run) -> bool {
+      const int other = set ^ 1;
+      if (!wait_all(&hand[other * 4 + quarter], (v >> 1) & 1)) return false;
+      const float m_o = sHand[other * kMlaRows + quarter * 32 + lane];
+      if (m_o > m_run) {
+        l_run *= exp2_approx(m_run - m_o);  // 0 when nothing was seen yet (m_run = -inf, l_run = 0)
+        m_run = m_o;
+      }
+      return true;
+    };
     uint32_t cur[kMlaUnit], nxt[kMlaUnit];
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = load_s(0, cur) && stage(0, cur);
-    for (int u = 0; ok && u < n_units; ++u) {
-      if (u + 1 < n_units && !(load_s(u + 1, nxt) && stage(u + 1, nxt))) {
-        ok = false;
-        break;
-      }
+    bool ok = set < n_units ? load_s(set, cur) && stage(set, cur) : true;
+    for (int u = set; ok && u < n_units; u += 2) {
       const int x = u % kMlaNX;
       if (!wait_all(&rx_full[x], (u / kMlaNX) & 1)) {
         ok = false;
@@ -655,6 +703,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       for (int c = 0; c < 16; ++c) mx[c & 3] = fmaxf(mx[c & 3], c < vis ? mine[c] * sgn : -INFINITY);
       float mxa = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 16));
+      // the max after unit u - 1 comes from the other set
+      if (u >= 1 && !catch_up(u - 1, m_run, l_run)) {
+        ok = false;
+        break;
+      }
       const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
       float alpha = 1.f;
       if (m_new > m_run + 8.0f) {
@@ -662,6 +715,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         m_run = m_new;
       }
       l_run *= alpha;
+      sHand[set * kMlaRows + quarter * 32 + lane] = m_run;
+      mbar_arrive(&hand[set * 4 + quarter]);  // release: the other set may take unit u + 1
+      // this set's next unit: scores from TMEM, the peer's heads staged (after this
+      // unit's receive, so the two CTAs' credits never wait on each other)
+      if (u + 2 < n_units && !(load_s(u + 2, nxt) && stage(u + 2, nxt))) {
+        ok = false;
+        break;
+      }
       const float neg_m = -m_run;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[8];
@@ -689,6 +750,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       mbar_arrive(&p_local[xp]);
 #pragma unroll
       for (int c = 0; c < kMlaUnit; ++c) cur[c] = nxt[c];
+    }
+    // the max after the last unit, for the set that did not process it
+    if (ok && ((n_units - 1) & 1) != set) ok = catch_up(n_units - 1, m_run, l_run);
+    float* sL = sHand + 2 * kMlaRows;
+    if (set == 1) {
+      // hand this set's share of the row sums to set 0, which writes the rows
+      sL[quarter * 32 + lane] = l_run;
+      mbar_arrive(fin);
+      ok = false;
+    } else if (ok && wait_all(fin, 0)) {
+      l_run += sL[quarter * 32 + lane];
+    } else {
+      ok = false;
     }
     if (ok && wait_all(&pv_done[(n_units - 1) % 4], ((n_units - 1) / 4) & 1)) {
       const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // the own head's row sum
@@ -880,6 +954,18 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   static int done = 0;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), MlaShape::kSmem, &done);
   if (rc) return rc;
+  // the warpgroups' register targets draw on the launch allocation: refuse to launch
+  // a build whose allocation is smaller (the raising warps would wait forever)
+  static int regs_checked = 0;
+  if (!regs_checked) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(mla_decode_kernel));
+    if (e != cudaSuccess) return fail(METIS_E_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+    if (fa.numRegs * kMlaThreads < 128 * (2 * kMlaRegsRow + 2 * kMlaRegsLow))
+      return fail(METIS_E_CUDA, "MLA kernel built with %d registers per thread, %d needed", fa.numRegs,
+                  (2 * kMlaRegsRow + 2 * kMlaRegsLow) / 4);
+    regs_checked = 1;
+  }
   rc = launch_dependent(mla_decode_kernel, dim3((unsigned)(lay.max_items * head_tiles * 2)), dim3(kMlaThreads),
                         MlaShape::kSmem, st, "mla_decode_kernel launch", tmKV, tmKVh, p);
   if (rc) return rc;
