@@ -9,8 +9,10 @@ step is one pass of the whole decode path over the batch: one decode call
 unsplit with the longest sequences first (``--partition P`` > 0 times the
 split-KV partial kernel and the log-sum-exp merge instead).  The KV cache
 (604 MB) is larger than L2, and
-L2 is additionally flushed (a 2x-L2 write) between timed steps, outside the
-timed events.
+L2 is additionally flushed between timed steps, outside the timed events, by
+reading a 2x-L2 buffer (``--flush write`` zeroes it instead; that leaves L2
+full of dirty lines whose write-back lands inside the next timed step, ~8 %
+slower; the line reports that variant under ``flush_reference``).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -55,6 +57,7 @@ WORKLOAD = ("batched paged decode, bf16 KV: 64 seqs, seq_lens U[512,4096], 32 q 
             "block_size 16, block_table a random permutation of the pool")
 PARTITION = 0      # unsplit: one CTA per (sequence, kv head), longest sequences first (no merge)
 MLA_PARTITION = 3072
+E2E_LAYERS = 4      # distinct layer caches the pipelined end-to-end leg cycles through
 NOMINAL_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth; fractions are reported against it and the measured peak
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TC_TFLOPS = (1900.0, 1700.0)
@@ -278,6 +281,23 @@ def run_reference(args, world, rank):
 # GPU leg
 # ---------------------------------------------------------------------------
 
+class L2Flush:
+    """Evicts L2 between timed steps, outside the timed events, by touching a buffer of
+    twice its size: "read" sums the buffer (L2 is left holding clean lines, as after a
+    model's weight reads), "write" zeroes it (L2 is left holding dirty lines, whose
+    write-back then falls inside the next timed step)."""
+
+    def __init__(self, nbytes, dev, mode):
+        self.buf = torch.zeros(nbytes // 4, dtype=torch.int32, device=dev)
+        self.mode = mode
+
+    def __call__(self):
+        if self.mode == "write":
+            self.buf.zero_()
+        else:
+            self.buf.sum(dtype=torch.int64)
+
+
 def run_ours(args, world, rank, local):
     import paged_attention_kv_decode_gb300 as pa
     from paged_attention_kv_decode_gb300 import workloads as wl
@@ -298,8 +318,7 @@ def run_ours(args, world, rank, local):
     part_out, part_lse = pa.split_workspace_views(ws, S, H, D, max_len, P) if P > 0 else (None, None)
     nbytes = decode_algorithmic_bytes(case)
     props = torch.cuda.get_device_properties(dev)
-    flush = torch.empty(max(2 * int(getattr(props, "L2_cache_size", 128 << 20)), 256 << 20), dtype=torch.uint8,
-                        device=dev)
+    flush = L2Flush(max(2 * int(getattr(props, "L2_cache_size", 128 << 20)), 256 << 20), dev, args.flush)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -340,7 +359,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     sampler.mark()
     for i in range(args.steps):
-        flush.zero_()                      # untimed: evict L2 between steps
+        flush()                      # untimed: evict L2 between steps
         starts[i].record(stream)
         ev_mid = mids[i]
         step()
@@ -356,6 +375,22 @@ def run_ours(args, world, rank, local):
     value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
     kern_avg_ms = float(np.mean(kern_ms))
     merge_avg_ms = float(np.mean([a - b for a, b in zip(step_ms, kern_ms)]))
+
+    # reference: the same steps with the other flush (untimed either way)
+    other = "write" if flush.mode == "read" else "read"
+    ref_flush = L2Flush(flush.buf.numel() * 4, dev, other)
+    ref_n = min(args.steps, 50)
+    r_s = [torch.cuda.Event(enable_timing=True) for _ in range(ref_n)]
+    r_e = [torch.cuda.Event(enable_timing=True) for _ in range(ref_n)]
+    for i in range(ref_n):
+        ref_flush()
+        r_s[i].record(stream)
+        ev_mid = mids[i]
+        step()
+        r_e[i].record(stream)
+    torch.cuda.synchronize()
+    ref_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(r_s, r_e)), world, dev)
+    del ref_flush
 
     # end to end through the public call: pinned host inputs -> device, decode, output -> pinned host
     h_q = case.q.pin_memory()
@@ -382,12 +417,39 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     for i in range(e2e_n):
-        flush.zero_()
+        flush()
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
-    sampler.stop()
     e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), world, dev)
+
+    # the same steps through the one-step-ahead pipeline: step k + 1's inputs go in and
+    # step k's output comes back while the decodes run.  Consecutive steps decode
+    # different layers (four caches of this shape, 2.4 GB), as a model's decode step
+    # would, so that nothing a step reads is still in L2 for the next and the steps
+    # can run back to back without a flush.
+    layers_k, layers_v = [kc], [vc]
+    gen = torch.Generator(device=dev).manual_seed(77)
+    for _ in range(E2E_LAYERS - 1):
+        layers_k.append(torch.randn(kc.shape, generator=gen, device=dev).to(kc.dtype))
+        layers_v.append(torch.randn(vc.shape, generator=gen, device=dev).to(vc.dtype))
+    pipe = pa.DecodePipeline(layers_k, layers_v, S, H, bt.shape[1], case.scale, max_len, partition_size=P, depth=2)
+    h_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    for i in range(3):
+        pipe.submit(h_q, h_bt, h_sl, h_outs[i % 2], layer=i % E2E_LAYERS)
+    pipe.synchronize()
+    barrier(world)
+    p_start = torch.cuda.Event(enable_timing=True)
+    p_end = torch.cuda.Event(enable_timing=True)
+    p_start.record(pipe.copy_in)
+    for i in range(e2e_n):
+        pipe.submit(h_q, h_bt, h_sl, h_outs[i % 2], layer=i % E2E_LAYERS)
+    p_end.record(pipe.copy_out)
+    pipe.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.stop()
+    pipe_ms = max_over_ranks(p_start.elapsed_time(p_end), world, dev)
     h2d = h_q.numel() * h_q.element_size() + h_bt.numel() * 4 + h_sl.numel() * 4
     d2h = h_out.numel() * h_out.element_size()
 
@@ -402,10 +464,13 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "partition_size": P, "tokens": int(case.seq_lens.sum()),
-                   "kv_bytes_per_step": nbytes, "l2": "inputs larger than L2 (KV 604 MB) and L2 flushed "
-                                                      "between timed steps (untimed 2x-L2 write)",
+                   "kv_bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2 (KV 604 MB) and L2 flushed between timed steps (untimed 2x-L2 "
+                         f"{flush.mode}: {'clean lines, as after weight reads' if flush.mode == 'read' else 'dirty lines, written back inside the next step'})",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": world * S * args.steps / (total_ms * 1e-3),
+        "flush_reference": {"flush": other, "value": world * nbytes * ref_n / (ref_ms * 1e-3) / 1e9,
+                            "ms_per_step": ref_ms / ref_n, "steps": ref_n},
         "hbm_frac": value / peak,
         "hbm_frac_nominal": value / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel", "achieved": achieved, "peak": peak,
@@ -413,10 +478,16 @@ def run_ours(args, world, rank, local):
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profiled_traffic(), "kernel_ms": kern_avg_ms, "merge_ms": merge_avg_ms if P > 0 else None,
                      "algorithmic_bytes_per_launch": nbytes},
-        "e2e": {"value": world * nbytes * e2e_n / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_n,
+        "e2e": {"value": world * nbytes * e2e_n / (pipe_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms / e2e_n,
                 "note": "KV cache resident in HBM; per step: q, block table, lengths H2D from pinned memory, "
-                        "output D2H to pinned memory"},
+                        "output D2H to pinned memory, through DecodePipeline (two slots: a step's copies "
+                        "overlap the neighbouring steps' decodes, each decode a replayed CUDA graph); "
+                        "consecutive steps decode four layers' caches in turn (2.4 GB, no L2 reuse), "
+                        "timed from the first copy to the last read-back",
+                "serial": {"value": world * nbytes * e2e_n / (e2e_ms * 1e-3) / 1e9, "ms_per_step": e2e_ms / e2e_n,
+                           "note": "the same step with copies, decode and read-back one after another on one "
+                                   "stream, L2 flushed between steps"}},
         "graph": graph_line,
         "gpu_launches": (2 if P > 0 else 1) * args.steps,
         "device_status": status,
@@ -454,7 +525,7 @@ def graph_replay(q, kc, vc, bt, sl, out, ws, scale, P, max_len, nbytes, steps, f
         ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         barrier(world)
         for i in range(steps):
-            flush.zero_()
+            flush()
             ev_s[i].record(cur)
             g.replay()
             ev_e[i].record(cur)
@@ -476,7 +547,7 @@ def _time_calls(call, reps, flush, stream):
     torch.cuda.synchronize()
     ts = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -655,6 +726,8 @@ def main():
                     help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw,pfx; "
                          "empty: none)")
     ap.add_argument("--workload-reps", type=int, default=20)
+    ap.add_argument("--flush", choices=["read", "write"], default="read",
+                    help="how L2 is evicted between timed steps (outside the timed events)")
     ap.add_argument("--ramp-steps", type=int, default=None,
                     help="untimed steps before warm-up (default: about one second of steps)")
     args = ap.parse_args()

@@ -43,3 +43,4 @@ from ._binding import (  # noqa: F401
     metis_reshape_and_cache,
     metis_version,
 )
+from .pipeline import DecodePipeline  # noqa: F401,E402
