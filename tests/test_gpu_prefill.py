@@ -152,3 +152,13 @@ def test_bad_block_id_and_q_len_are_flagged():
                          seq_lens=torch.tensor([10, 15], dtype=torch.int32), scale=case.scale)
     gpu_prefill(bad, max_seq_len=60)
     assert pa.metis_read_status() & pa.STATUS_BAD_Q_LEN
+
+
+def test_empty_chunks_and_more_units_than_ctas():
+    """Chunks of 0 tokens (nothing to compute: the unit fetcher skips them) between real
+    ones, and more (item, KV head) units than SMs, taken from the list as the CTAs free up."""
+    prefixes = [0, 300, 50, 0, 1000, 7, 0, 129] * 6
+    q_lens = [40, 0, 300, 0, 1, 0, 64, 200] * 6
+    case = wl.make_prefill_case(61, prefixes, q_lens, H=32, G=8, D=128, bs=16, dtype=torch.bfloat16,
+                                extra_blocks=4, poison=True)
+    check(case)
