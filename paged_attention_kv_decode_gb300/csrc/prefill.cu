@@ -73,7 +73,12 @@ constexpr int kRegsProd = PF_REGS_PROD;        // warpgroup 2: K/V producers
 constexpr int kRegsMma = PF_REGS_MMA;          // warpgroup 3: UMMA issuer, query loader, idle warps
 static_assert(128 * (2 * kRegsSoftmax + kRegsProd + kRegsMma) <= kPfThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
-constexpr int kKStages = 3;       // K ring depth (V ring: 2)
+#ifndef METIS_PF_K_STAGES
+#define METIS_PF_K_STAGES 3
+#define METIS_PF_V_STAGES 2
+#endif
+constexpr int kKStages = METIS_PF_K_STAGES;  // K ring depth
+constexpr int kVStages = METIS_PF_V_STAGES;  // V ring depth
 constexpr int kKvTile = 128;      // tokens per K/V tile
 constexpr int kRows = 128;        // query rows per tile
 constexpr int kTmemCols = 512;    // S0 | S1 | O0 | O1
@@ -102,13 +107,29 @@ struct PfShape {
   static constexpr int kKvBytes = kHalves * kKvHalf;
   static constexpr int kQ = 0;                                 // 2 query tiles
   static constexpr int kK = kQ + 2 * kQBytes;                  // kKStages stages
-  static constexpr int kV = kK + kKStages * kKvBytes;          // 2 stages
-  static constexpr int kTiles = kV + 2 * kKvBytes;             // 224 KB at head_dim 128
+  static constexpr int kV = kK + kKStages * kKvBytes;          // kVStages stages
+  static constexpr int kTiles = kV + kVStages * kKvBytes;      // 224 KB at head_dim 128
   // + 1 KB: the barriers live in the alignment slack (below the aligned base when it
   // is at least 256 B, else just past the tiles).  At least 120 KB so that one CTA
   // (all 512 TMEM columns) is resident per SM.
   static constexpr int kSmem = (kTiles + 1024) > 120 * 1024 ? (kTiles + 1024) : 120 * 1024;
 };
+
+// mbarrier layout (indices into the barrier area) and arrival counts
+struct PfBar {
+  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = kKFull + kKStages, kVFull = kKEmpty + kKStages,
+                       kVEmpty = kVFull + kVStages, kSFull = kVEmpty + kVStages, kPFull = kSFull + 2,
+                       kPvDone = kPFull + 2, kDrain = kPvDone + 2, kQFree = kDrain + 1, kUnitFull = kQFree + 1,
+                       kUnitEmpty = kUnitFull + 2, kCount = kUnitEmpty + 2;
+  // full barriers: one arrival per producer warp of the ring; p_full: 128 softmax threads
+  __host__ __device__ static constexpr int arrivals(int i) {
+    return (i >= kPFull && i < kPFull + 2) ? 128
+           : ((i >= kKFull && i < kKFull + kKStages) || (i >= kVFull && i < kVFull + kVStages)) ? 2
+           : (i >= kUnitEmpty && i < kUnitEmpty + 2) ? kUnitReaders
+                                                      : 1;
+  }
+};
+static_assert((PfBar::kCount + 4) * 8 <= 256, "prefill barrier area");
 
 // Effective (sequence length, query count) after clamping to what can be read.
 __device__ __forceinline__ void pf_lengths(const PrefillParams& p, int s, int& L, int& q_len, bool flag) {
@@ -235,21 +256,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   uint8_t* sK = smem + Sh::kK;
   uint8_t* sV = smem + Sh::kV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(slack >= 256 ? smem - 256 : smem + Sh::kTiles);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [kKStages]
-  uint64_t* k_empty = bars + 4;   // [kKStages]
-  uint64_t* v_full = bars + 7;    // [2 stages]
-  uint64_t* v_empty = bars + 9;   // [2 stages]
-  uint64_t* s_full = bars + 11;   // [2 groups] QK_w_j landed in S_w
-  uint64_t* p_full = bars + 13;   // [2 groups] P_w_j written over S_w (128 arrivals)
-  uint64_t* pv_done = bars + 15;  // [2 groups] PV_w_j completed
-  uint64_t* drain = bars + 17;
-  uint64_t* q_free = bars + 18;   // every QK of a unit completed: its query tiles may be replaced
-  uint64_t* unit_full = bars + 19;   // [2] a unit index published
-  uint64_t* unit_empty = bars + 21;  // [2] every consuming warp has read it (kUnitReaders arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 24);
-  volatile int* unit_slot = reinterpret_cast<volatile int*>(bars + 25);  // [2]
+  uint64_t* q_full = bars + PfBar::kQFull;
+  uint64_t* k_full = bars + PfBar::kKFull;      // [kKStages]
+  uint64_t* k_empty = bars + PfBar::kKEmpty;    // [kKStages]
+  uint64_t* v_full = bars + PfBar::kVFull;      // [kVStages]
+  uint64_t* v_empty = bars + PfBar::kVEmpty;    // [kVStages]
+  uint64_t* s_full = bars + PfBar::kSFull;      // [2 groups] QK_w_j landed in S_w
+  uint64_t* p_full = bars + PfBar::kPFull;      // [2 groups] P_w_j written over S_w (128 arrivals)
+  uint64_t* pv_done = bars + PfBar::kPvDone;    // [2 groups] PV_w_j completed
+  uint64_t* drain = bars + PfBar::kDrain;
+  uint64_t* q_free = bars + PfBar::kQFree;      // every QK of a unit completed: its query tiles may be replaced
+  uint64_t* unit_full = bars + PfBar::kUnitFull;    // [2] a unit index published
+  uint64_t* unit_empty = bars + PfBar::kUnitEmpty;  // [2] every consuming warp has read it (kUnitReaders arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PfBar::kCount);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + PfBar::kCount + 1);
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(bars + PfBar::kCount + 2);  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = *p.item_count * p.G;
@@ -257,10 +278,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
 
   if (threadIdx.x == 0) {
     // full barriers: one arrival per producer warp of the ring; p_full: 128 softmax threads
-    for (int i = 0; i < 23; ++i)
-      mbar_init(&bars[i], (i == 13 || i == 14) ? 128
-                          : ((i >= 1 && i <= 3) || (i >= 7 && i <= 8)) ? 2
-                          : (i >= 21) ? kUnitReaders : 1);
+    for (int i = 0; i < PfBar::kCount; ++i) mbar_init(&bars[i], PfBar::arrivals(i));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -304,7 +322,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   };
 
   // Ring positions run on across units: K/V tile t (counted over every unit this
-  // CTA has processed) sits in K stage t % kKStages and V stage t % 2, and each
+  // CTA has processed) sits in K stage t % kKStages and V stage t % kVStages, and each
   // barrier's phase is the number of its earlier completions.
   if (warp >= 8 && warp < kMmaWarp) {
     // ------------------------------------------------------------ K/V producers
@@ -319,7 +337,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     const int npg = kKvTile / p.bs;            // pages per K/V tile (2, 4 or 8)
     const int half_pg = npg >> 1;              // pages of this warp
     const uint64_t pol = l2_policy_evict_last();
-    const int depth = is_k ? kKStages : 2;
+    const int depth = is_k ? kKStages : kVStages;
     if (lane == 0) tma_prefetch_desc(map);
     uint32_t t = 0, k = 0;                     // tiles issued so far, units read
     bool ok = true;
@@ -375,7 +393,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     };
     auto pv = [&](int w, uint32_t t, bool first) {  // O_w (+)= P_w V_t, P_w from the first 64 columns of S_w
       if (lane == 0) {
-        const uint32_t vbase = smem_u32(sV + (t & 1) * Sh::kKvBytes);
+        const uint32_t vbase = smem_u32(sV + (t % kVStages) * Sh::kKvBytes);
         const uint32_t o_tmem = tmem + 2 * kKvTile + w * D;
 #pragma unroll
         for (int kk = 0; kk < kKvTile / 16; ++kk)
@@ -410,8 +428,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
       __syncwarp();
       for (int j = 0; ok && j < it.n_kv; ++j) {
         const uint32_t t = t_base + j;
-        const int vst = t & 1;
-        if (!wait_all(&v_full[vst], (t >> 1) & 1)) {
+        const int vst = t % kVStages;
+        if (!wait_all(&v_full[vst], (t / kVStages) & 1)) {
           ok = false;
           break;
         }
