@@ -116,3 +116,16 @@ def test_bad_block_id_is_flagged():
     assert torch.isfinite(out.float()).all()
     ref_o, _ = oracle_mla(case)
     assert_parity(out[1:], ref_o[1:], torch.bfloat16)
+
+
+def test_more_items_than_the_schedule_sorts():
+    """2100 short sequences, unsplit: more work items than the schedule kernel sorts (2048)."""
+    rng = np.random.default_rng(8)
+    case = wl.make_mla_case(63, list(rng.integers(1, 40, 2100)), H=16, bs=16, poison=True, extra_blocks=2)
+    ref_o, ref_l = oracle.mla_decode(case.q, case.kv_cache, case.block_table, case.seq_lens, case.scale)
+    out, lse = pa.metis_mla_decode(dev(case.q), dev(case.kv_cache), dev(case.block_table), dev(case.seq_lens),
+                                   case.scale, partition_size=0, max_seq_len=case.max_seq_len, want_lse=True)
+    torch.cuda.synchronize()
+    assert_parity(out, ref_o, torch.bfloat16)
+    assert_lse(lse, ref_l, torch.bfloat16)
+    assert pa.metis_read_status() == 0

@@ -162,3 +162,13 @@ def test_empty_chunks_and_more_units_than_ctas():
     case = wl.make_prefill_case(61, prefixes, q_lens, H=32, G=8, D=128, bs=16, dtype=torch.bfloat16,
                                 extra_blocks=4, poison=True)
     check(case)
+
+
+def test_more_items_than_the_schedule_sorts():
+    """2100 single-token sequences: more work items than the schedule kernel sorts in shared
+    memory (2048), so they run in list order."""
+    rng = np.random.default_rng(7)
+    n = 2100
+    case = wl.make_prefill_case(62, list(rng.integers(0, 40, n)), [1] * n, H=8, G=2, D=64, bs=16,
+                                dtype=torch.bfloat16, extra_blocks=3, poison=True)
+    check(case)
