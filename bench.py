@@ -603,10 +603,44 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
             ql = int(cu[si + 1] - cu[si])
             flops += int(((lens[si] - ql) + np.arange(ql) + 1).sum()) * c.H * 4 * c.D
         tf = flops / med / 1e9
+        qlen = np.diff(cu)
+        kv_bytes = int(lens.astype(np.int64).sum()) * c.G * c.D * 2 * 2
+        io_bytes = 2 * c.T * c.H * c.D * 2                       # q in, out
+        flop_ms = flops / (tc_burst * 1e9)
+        byte_ms = (kv_bytes + io_bytes) / (peak_hbm * 1e6)
+
+        def sub_call(sel):
+            # the same call over a subset of the sequences (the chunks, or the decodes)
+            rows = np.concatenate([np.arange(cu[si], cu[si + 1]) for si in sel])
+            sq = c.q[torch.from_numpy(rows)].contiguous().to(dev)
+            scu = torch.from_numpy(np.concatenate([[0], np.cumsum(qlen[sel])]).astype(np.int32)).to(dev)
+            sbt = c.block_table[torch.from_numpy(sel)].contiguous().to(dev)
+            ssl = c.seq_lens[torch.from_numpy(sel)].contiguous().to(dev)
+            sout = torch.empty_like(sq)
+            sws = torch.empty(pa.metis_prefill_workspace_bytes(len(sel), len(rows), c.H, c.G), dtype=torch.uint8,
+                              device=dev)
+            sm, _ = _time_calls(lambda: pa.metis_paged_attn_prefill_chunk(sq, scu, t[2], t[3], sbt, ssl, c.scale,
+                                                                          out=sout, max_seq_len=c.max_seq_len,
+                                                                          workspace=sws, stream=stream),
+                                reps, flush, stream)
+            sflops = sum(int(((lens[si] - qlen[si]) + np.arange(qlen[si]) + 1).sum()) for si in sel) * c.H * 4 * c.D
+            skv = int(lens[sel].astype(np.int64).sum()) * c.G * c.D * 2 * 2
+            return sm, sflops, skv
+
+        ch_ms, ch_flops, _ = sub_call(np.where(qlen > 1)[0])
+        de_ms, _, de_kv = sub_call(np.where(qlen == 1)[0])
         res["chunked_prefill"] = {"ms": med, "TFLOP_s": tf, "tensor_frac_burst": tf / tc_burst,
                                   "tensor_frac_sustained": tf / tc_sus, "flops": flops, "tokens": c.T,
                                   "tokens_per_s": c.T / (med * 1e-3),
-                                  "note": "one call: 16 chunks of 512 over cached prefixes + 48 single-token decodes"}
+                                  "flop_bound_ms": flop_ms, "byte_bound_ms": byte_ms,
+                                  "roofline_frac": max(flop_ms, byte_ms) / med,
+                                  "chunks_alone": {"ms": ch_ms, "TFLOP_s": ch_flops / ch_ms / 1e9,
+                                                   "tensor_frac_burst": ch_flops / ch_ms / 1e9 / tc_burst},
+                                  "decodes_alone": {"ms": de_ms, "GB_s": de_kv / de_ms / 1e6,
+                                                    "hbm_frac": de_kv / de_ms / 1e6 / peak_hbm},
+                                  "note": "one call: 16 chunks of 512 over cached prefixes + 48 single-token decodes; "
+                                          "roofline_frac = max(flop bound, byte bound) / call time; the two kinds "
+                                          "also timed as calls of their own"}
         del t, out, ws, c
         torch.cuda.empty_cache()
     if "kvw" in names:
