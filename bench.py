@@ -570,8 +570,20 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         med, mn = _time_calls(lambda: pa.metis_paged_attn_decode(*t, c.scale, out=out, max_seq_len=c.max_seq_len,
                                                                   stream=stream), reps, flush, stream)
         nb = decode_algorithmic_bytes(c)
-        res["tiny_decode_fp32"] = {"ms": med, "GB_s": nb / med / 1e6, "kv_bytes": nb,
-                                   "note": "about 67 KB of KV: launch-latency bound"}
+        # the same call captured as a CUDA graph: the device time without the host's issue time
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            pa.metis_paged_attn_decode(*t, c.scale, out=out, max_seq_len=c.max_seq_len)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            pa.metis_paged_attn_decode(*t, c.scale, out=out, max_seq_len=c.max_seq_len)
+        torch.cuda.synchronize()
+        gmed, _ = _time_calls(g.replay, reps, flush, stream)
+        res["tiny_decode_fp32"] = {"ms": med, "GB_s": nb / med / 1e6, "graph_ms": gmed, "kv_bytes": nb,
+                                   "note": "about 67 KB of KV: launch-latency bound (ms: issued from Python; "
+                                           "graph_ms: replayed as a CUDA graph)"}
     if "c3" in names:
         c = wl.config3_long_split_decode()
         t = [x.to(dev) for x in (c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]

@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
 // ---------------------------------------------------------------------------
 // fp32 decode on FMA units
 // ---------------------------------------------------------------------------
-constexpr int kF32Warps = 4;
+constexpr int kF32Warps = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float* __restrict__ k_cache,
@@ -425,35 +425,51 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
   }
   const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
   const size_t row_stride = (size_t)p.G * D;
-  for (int t = t0 + warp; t < t1; t += kF32Warps) {
-    const int page = t / p.bs;
-    const int b = checked_block(bt_row, page, p.num_blocks, &g_status_decode);
-    float kv[DPL], vv[DPL];
-    if (b >= 0) {
-      const size_t off = ((size_t)b * p.bs + (t - page * p.bs)) * row_stride + (size_t)g * D + lane * DPL;
+  // The warp's tokens t0 + warp, + kF32Warps, ... in groups of kF32Batch: the block ids
+  // and K/V rows of a group are loaded together, then folded in one at a time in token
+  // order (the same order as without grouping).
+  constexpr int kF32Batch = D == 64 ? 8 : 4;
+  for (int tb = t0 + warp; tb < t1; tb += kF32Batch * kF32Warps) {
+    float kv[kF32Batch][DPL], vv[kF32Batch][DPL];
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) {
-        kv[i] = __ldg(k_cache + off + i);
-        vv[i] = __ldg(v_cache + off + i);
+    for (int u = 0; u < kF32Batch; ++u) {
+      const int t = tb + u * kF32Warps;
+      int b = -1, page = 0;
+      if (t < t1) {
+        page = t / p.bs;
+        b = checked_block(bt_row, page, p.num_blocks, &g_status_decode);
       }
-    } else {
+      if (b >= 0) {
+        const size_t off = ((size_t)b * p.bs + (t - page * p.bs)) * row_stride + (size_t)g * D + lane * DPL;
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) kv[i] = vv[i] = 0.f;
+        for (int i = 0; i < DPL; ++i) {
+          kv[u][i] = __ldg(k_cache + off + i);
+          vv[u][i] = __ldg(v_cache + off + i);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) kv[u][i] = vv[u][i] = 0.f;
+      }
     }
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      if (h >= p.r) break;
-      float dot = 0.f;
+    for (int u = 0; u < kF32Batch; ++u) {
+      if (tb + u * kF32Warps >= t1) break;
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) dot = fmaf(qv[h][i], kv[i], dot);
-      dot = warp_sum_xor(dot, 1);
-      const float mn = fmaxf(m[h], dot);
-      const float al = exp2_approx(m[h] - mn);
-      const float pr = exp2_approx(dot - mn);
-      l[h] = l[h] * al + pr;
+      for (int h = 0; h < 8; ++h) {
+        if (h < p.r) {
+          float dot = 0.f;
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) o[h][i] = fmaf(pr, vv[i], o[h][i] * al);
-      m[h] = mn;
+          for (int i = 0; i < DPL; ++i) dot = fmaf(qv[h][i], kv[u][i], dot);
+          dot = warp_sum_xor(dot, 1);
+          const float mn = fmaxf(m[h], dot);
+          const float al = exp2_approx(m[h] - mn);
+          const float pr = exp2_approx(dot - mn);
+          l[h] = l[h] * al + pr;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) o[h][i] = fmaf(pr, vv[u][i], o[h][i] * al);
+          m[h] = mn;
+        }
+      }
     }
   }
   if (lane == 0) {
