@@ -27,13 +27,16 @@ def steps_of(case, n, seed):
     return out
 
 
-@pytest.mark.parametrize("depth,use_graph", [(2, True), (2, False), (1, True), (3, True)])
-def test_every_step_matches_the_oracle(depth, use_graph):
+@pytest.mark.parametrize("depth,use_graph,partition", [(2, True, 0), (2, False, 0), (1, True, 0), (3, True, 0),
+                                                       (2, True, 128), (2, False, 64)])
+def test_every_step_matches_the_oracle(depth, use_graph, partition):
+    """Depths 1-3, graphs on and off, unsplit and split-KV (decode + merge in each slot's graph)."""
     case = wl.config2_batched_decode(poison=True, num_seqs=6, len_lo=1, len_hi=600, extra_blocks=2)
     dev = torch.device("cuda")
     S, H, D = case.q.shape
     pipe = pa.DecodePipeline(case.k_cache.to(dev), case.v_cache.to(dev), S, H, case.block_table.shape[1],
-                             case.scale, case.max_seq_len, depth=depth, use_graph=use_graph)
+                             case.scale, case.max_seq_len, partition_size=partition, depth=depth,
+                             use_graph=use_graph)
     steps = steps_of(case, 7, 11 + depth)
     host_in = [(q.pin_memory(), bt.pin_memory(), sl.pin_memory()) for q, bt, sl in steps]
     host_out = [torch.empty(S, H, D, dtype=case.q.dtype).pin_memory() for _ in steps]
