@@ -590,15 +590,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-        if (lean) {
-#pragma unroll
-          for (int c = 0; c < kKvTile; c += 2)
-            mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-        } else {
+        if (!lean) {
+          // fold the mask (a select: NaN-safe) and a negative scale's sign into the
+          // scores once, so that one code path serves every tile
 #pragma unroll
           for (int c = 0; c < kKvTile; ++c)
-            mx[c & 7] = fmaxf(mx[c & 7], c < vis ? __uint_as_float(sv[c]) * sgn : -INFINITY);
+            sv[c] = c < vis ? __float_as_uint(__uint_as_float(sv[c]) * sgn) : 0xff800000u;
         }
+#pragma unroll
+        for (int c = 0; c < kKvTile; c += 2)
+          mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
         const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
         const bool grow = m_new > m_run + 8.0f;   // rescale only when the max grew past 2^8
@@ -625,25 +626,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
         const float neg_m = -m_run;
         uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // row sums, as packed pairs
         const uint64_t asl2_2 = f2_pack(asl2, asl2), neg_m2 = f2_pack(neg_m, neg_m);
-        if (lean) {
-          // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
+        // per pair: one packed FMA, two exponentials, one packed add, one bf16x2 convert
+        // (a hidden key is -inf here and m_run is finite after tile 0, where every row sees
+        // key 0: its exponential is exactly 0)
 #pragma unroll
-          for (int c = 0; c < kKvTile; c += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
-            const float e0 = exp2_approx(x0);
-            const float e1 = exp2_approx(x1);
-            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
-            sv[c >> 1] = pack_bf16x2(e0, e1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kKvTile; c += 2) {
-            const float e0 = c < vis ? exp2_approx(fmaf(__uint_as_float(sv[c]) * sgn, asl2, neg_m)) : 0.f;
-            const float e1 = c + 1 < vis ? exp2_approx(fmaf(__uint_as_float(sv[c + 1]) * sgn, asl2, neg_m)) : 0.f;
-            ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
-            sv[c >> 1] = pack_bf16x2(e0, e1);
-          }
+        for (int c = 0; c < kKvTile; c += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), asl2_2, neg_m2), x0, x1);
+          const float e0 = exp2_approx(x0);
+          const float e1 = exp2_approx(x1);
+          ls2[(c >> 1) & 3] = f2_add(ls2[(c >> 1) & 3], f2_pack(e0, e1));
+          sv[c >> 1] = pack_bf16x2(e0, e1);
         }
         tmem_st32(s_tmem, sv);
         tmem_st32(s_tmem + 32, sv + 32);
