@@ -53,6 +53,16 @@ def test_single_sequence(prefix, q_len):
     check(case)
 
 
+@pytest.mark.parametrize("scale", [-0.0883883, 0.0, 1.0, -2.0])
+def test_scale_sign_and_size(scale):
+    """A negative scale (the sign folded into the scores), a zero scale (uniform weights
+    over the visible keys) and large scales (the running max grows past 2^8 on later
+    tiles, so O is rescaled), on chunks whose diagonal tiles hide part of each row."""
+    case = wl.make_prefill_case(61, [0, 200, 1000, 90], [300, 129, 64, 1], H=32, G=8, D=128, bs=16,
+                                dtype=torch.bfloat16, scale=scale, extra_blocks=3, poison=True)
+    check(case)
+
+
 @pytest.mark.parametrize("D,bs,H,G", [(128, 32, 32, 8), (128, 64, 16, 16), (64, 16, 16, 8), (64, 64, 8, 1),
                                       (128, 16, 16, 1), (128, 16, 32, 4)])
 def test_shapes(D, bs, H, G):
