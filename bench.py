@@ -32,7 +32,11 @@ bounded sample of the same workload instead.
 
 import os
 
-# The oracle legs run single-threaded: say so and make it so (before numpy loads BLAS).
+# The oracle legs spread sequences over a pool of threads, one per host core
+# (NumPy and torch release the GIL in the gathers and products); each product
+# is small (4 rows x a few thousand keys), and a multi-threaded BLAS on such
+# products measured ~10x slower than one thread, so BLAS runs single-threaded
+# inside each worker (set before numpy loads BLAS).
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -215,10 +219,34 @@ def max_over_ranks(x: float, world: int, device) -> float:
 # CPU oracle legs
 # ---------------------------------------------------------------------------
 
-def oracle_step(case, seqs):
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_step(case, seqs, pool=None):
+    """The oracle, as it stands, over the listed sequences: one call per sequence, spread over `pool`.
+    Returns the per-sequence ``(out [1, H, D], lse [1, H])`` in the order of `seqs`."""
     import oracle
-    oracle.paged_decode(case.q[seqs], case.k_cache, case.v_cache, case.block_table[seqs], case.seq_lens[seqs],
-                        case.scale)
+
+    def one(s):
+        sl = slice(int(s), int(s) + 1)
+        return oracle.paged_decode(case.q[sl], case.k_cache, case.v_cache, case.block_table[sl], case.seq_lens[sl],
+                                   case.scale)
+
+    if pool is None:
+        return [one(s) for s in seqs]
+    return list(pool.map(one, list(seqs)))
+
+
+# Parity bar: fp32 max |d| <= 1e-5; bf16 inputs |d| <= 1.5e-2 + 1e-2 |ref| elementwise.
+def error_summary(got: torch.Tensor, ref: np.ndarray, fp32: bool) -> dict:
+    """Max abs error of a GPU output against the oracle's, and the worst error as a fraction of the bar."""
+    g = got.detach().to("cpu", torch.float64).numpy()
+    d = np.abs(g - ref)
+    bound = np.full_like(ref, 1e-5) if fp32 else 1.5e-2 + 1e-2 * np.abs(ref)
+    ratio = float((d / bound).max()) if d.size else 0.0
+    return {"max_abs_err": float(d.max()) if d.size else 0.0, "tol": "1e-5 abs" if fp32 else "1.5e-2 + 1e-2 |ref|",
+            "tol_ratio": ratio, "within_tol": bool(np.isfinite(g).all() and ratio <= 1.0), "outputs_checked": int(d.size)}
 
 
 def sub_bytes(case, seqs) -> int:
@@ -228,50 +256,74 @@ def sub_bytes(case, seqs) -> int:
     return decode_algorithmic_bytes(sub)
 
 
-def cpu_baseline(case, budget_s=10.0):
-    """The oracle, as it stands, on the whole batch repeated until ~budget_s of CPU work."""
-    seqs = np.arange(case.S)
-    nbytes = decode_algorithmic_bytes(case)
+def _timed_passes(case, seqs, budget_s, pool):
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle_step(case, seqs)
+        oracle_step(case, seqs, pool)
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"the full 64-sequence batch, {reps} pass(es), float64 NumPy, {dt:.1f} s wall"}
+    return reps, time.perf_counter() - t0
+
+
+def cpu_baseline(case, budget_s=10.0, gpu_out=None):
+    """The oracle, as it stands, on the whole batch repeated until ~budget_s of wall time, its sequences
+    spread over one thread per host core; the same on one thread is reported beside it.  With `gpu_out`,
+    the oracle's output of the batch is also the parity reference of the GPU step's output."""
+    from concurrent.futures import ThreadPoolExecutor
+    torch.set_num_threads(1)
+    seqs = np.arange(case.S)
+    nbytes = decode_algorithmic_bytes(case)
+    cores = host_cores()
+    with ThreadPoolExecutor(cores) as pool:
+        reps, dt = _timed_passes(case, seqs, budget_s, pool)
+        parity = None
+        if gpu_out is not None:
+            ref = np.concatenate([o for o, _ in oracle_step(case, seqs, pool)])
+            parity = error_summary(gpu_out, ref, case.dtype == torch.float32)
+    reps1, dt1 = _timed_passes(case, seqs, budget_s / 2, None)
+    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "parity_of_gpu_output": parity,
+            "sample": f"the full 64-sequence batch, {reps} pass(es) in {dt:.1f} s wall, one oracle call per "
+                      f"sequence over {cores} threads (float64 NumPy, BLAS single-threaded per call)",
+            "single_thread": {"value": nbytes * reps1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"the same batch, {reps1} pass(es) in {dt1:.1f} s on one thread"}}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
+    from concurrent.futures import ThreadPoolExecutor
     from paged_attention_kv_decode_gb300 import workloads as wl
+    torch.set_num_threads(1)
     case = wl.config2_batched_decode()
+    cores = host_cores()
     rng = np.random.default_rng(0)
-    t0 = time.perf_counter()
-    oracle_step(case, np.arange(1))
-    per_seq = max(time.perf_counter() - t0, 1e-3)
-    budget = 150.0
-    n = int(max(1, min(case.S, budget / max(1, args.steps + args.warmup) / per_seq)))
-    samples = [rng.choice(case.S, size=n, replace=False) for _ in range(args.steps + args.warmup)]
-    for i in range(args.warmup):
-        oracle_step(case, samples[i])
-    tot_bytes = 0
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        s = samples[args.warmup + i]
-        oracle_step(case, s)
-        tot_bytes += sub_bytes(case, s)
-    dt = time.perf_counter() - t0
+    with ThreadPoolExecutor(cores) as pool:
+        t0 = time.perf_counter()
+        oracle_step(case, np.arange(min(cores, case.S)), pool)
+        per_seq = max((time.perf_counter() - t0) / min(cores, case.S), 1e-4)
+        budget = 150.0
+        n = int(max(1, min(case.S, budget / max(1, args.steps + args.warmup) / per_seq)))
+        samples = [rng.choice(case.S, size=n, replace=False) for _ in range(args.steps + args.warmup)]
+        for i in range(args.warmup):
+            oracle_step(case, samples[i], pool)
+        tot_bytes = 0
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            s = samples[args.warmup + i]
+            oracle_step(case, s, pool)
+            tot_bytes += sub_bytes(case, s)
+        dt = time.perf_counter() - t0
     value = tot_bytes / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample_seqs_per_step": n},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n} of 64 sequences per step (random), float64 NumPy"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} of 64 sequences per step (random), one oracle call per sequence over "
+                                       f"{cores} threads, float64 NumPy"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -484,7 +536,9 @@ def run_ours(args, world, rank, local):
                         "output D2H to pinned memory, through DecodePipeline (two slots: a step's copies "
                         "overlap the neighbouring steps' decodes, each decode a replayed CUDA graph); "
                         "consecutive steps decode four layers' caches in turn (2.4 GB, no L2 reuse), "
-                        "timed from the first copy to the last read-back",
+                        "timed from the first copy to the last read-back; unlike `value`, NO L2 flush runs "
+                        "between these steps (they run back to back), so a step may start while the previous "
+                        "one drains",
                 "serial": {"value": world * nbytes * e2e_n / (e2e_ms * 1e-3) / 1e9, "ms_per_step": e2e_ms / e2e_n,
                            "note": "the same step with copies, decode and read-back one after another on one "
                                    "stream, L2 flushed between steps"}},
@@ -496,11 +550,13 @@ def run_ours(args, world, rank, local):
     if args.workloads:
         (tcb, tcs), tc_src = load_tc_peaks()
         names = [w.strip() for w in args.workloads.split(",") if w.strip()]
-        line["workloads"] = other_workloads(names, args.workload_reps, dev, flush, stream, peak, (tcb, tcs))
+        line["workloads"] = other_workloads(names, args.workload_reps, dev, flush, stream, peak, (tcb, tcs),
+                                            oracle_legs=not args.no_cpu_baseline, c3_seqs=args.c3_seqs)
         line["workloads"]["peaks"] = {"hbm_GB_s": peak, "bf16_TFLOP_s_burst": tcb, "bf16_TFLOP_s_sustained": tcs,
                                       "source": tc_src}
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case)
+        line["cpu_baseline"] = cpu_baseline(case, gpu_out=out)
+        line["max_abs_err"] = line["cpu_baseline"]["parity_of_gpu_output"]["max_abs_err"]
     print(json.dumps(line), flush=True)
     return 0
 
@@ -541,7 +597,12 @@ def graph_replay(q, kc, vc, bt, sl, out, ws, scale, P, max_len, nbytes, steps, f
 # the other workloads: timed the same way (events, untimed L2 flush between reps)
 # ---------------------------------------------------------------------------
 
-def _time_calls(call, reps, flush, stream):
+def _time_calls(call, reps, flush, stream, name=None):
+    """Median and min event time of `call` over `reps` (3 untimed calls first, L2 flushed before each
+    timed one).  With `name`, the calls sit in an NVTX range of that name, so a profiler can pick out
+    this workload's launches (ncu --nvtx --nvtx-include "<name>/")."""
+    if name:
+        torch.cuda.nvtx.range_push(name)
     for _ in range(3):
         call()
     torch.cuda.synchronize()
@@ -555,10 +616,28 @@ def _time_calls(call, reps, flush, stream):
         b.record(stream)
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
+    if name:
+        torch.cuda.nvtx.range_pop()
     return float(np.median(ts)), float(np.min(ts))
 
 
-def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
+def oracle_leg(items, fn, work, unit, fp32, gpu_out, note):
+    """CPU leg of a workload: the oracle, as it stands, called once per item (a sequence, or a sub-batch of
+    one sequence) over one thread per host core, timed; its output is the parity reference of `gpu_out`
+    (rows in item order).  `work` is the workload's work in `unit` x 1e9 (bytes or flops)."""
+    from concurrent.futures import ThreadPoolExecutor
+    torch.set_num_threads(1)
+    cores = host_cores()
+    with ThreadPoolExecutor(cores) as pool:
+        t0 = time.perf_counter()
+        res = list(pool.map(fn, items))
+        dt = time.perf_counter() - t0
+    ref = np.concatenate(res)
+    return {"value": work / dt / 1e9, "unit": unit, "cores": cores, "kind": "oracle", "wall_s": dt,
+            "sample": note, "parity_of_gpu_output": error_summary(gpu_out, ref, fp32)}
+
+
+def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc, oracle_legs=True, c3_seqs=8):
     import paged_attention_kv_decode_gb300 as pa
     from paged_attention_kv_decode_gb300 import workloads as wl
     res = {}
@@ -568,7 +647,8 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         t = [x.to(dev) for x in (c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
         out = torch.empty_like(t[0])
         med, mn = _time_calls(lambda: pa.metis_paged_attn_decode(*t, c.scale, out=out, max_seq_len=c.max_seq_len,
-                                                                  stream=stream), reps, flush, stream)
+                                                                  stream=stream), reps, flush, stream,
+                              "tiny_decode_fp32")
         nb = decode_algorithmic_bytes(c)
         # the same call captured as a CUDA graph: the device time without the host's issue time
         side = torch.cuda.Stream()
@@ -584,20 +664,35 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         res["tiny_decode_fp32"] = {"ms": med, "GB_s": nb / med / 1e6, "graph_ms": gmed, "kv_bytes": nb,
                                    "note": "about 67 KB of KV: launch-latency bound (ms: issued from Python; "
                                            "graph_ms: replayed as a CUDA graph)"}
+        if oracle_legs:
+            import oracle
+            res["tiny_decode_fp32"]["cpu_baseline"] = oracle_leg(
+                range(c.S), lambda si: oracle.paged_decode(c.q[si:si + 1], c.k_cache, c.v_cache,
+                                                           c.block_table[si:si + 1], c.seq_lens[si:si + 1],
+                                                           c.scale)[0],
+                nb, "GB/s", True, out, "every sequence, one oracle call each")
     if "c3" in names:
-        c = wl.config3_long_split_decode()
+        c = wl.config3_long_split_decode(num_seqs=c3_seqs)
         t = [x.to(dev) for x in (c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
         out = torch.empty_like(t[0])
         ws = torch.empty(pa.metis_decode_workspace_bytes(c.S, c.H, c.D, c.max_seq_len, c.partition_size),
                          dtype=torch.uint8, device=dev)
         med, mn = _time_calls(lambda: pa.metis_paged_attn_decode(*t, c.scale, out=out, partition_size=c.partition_size,
                                                                   max_seq_len=c.max_seq_len, workspace=ws,
-                                                                  stream=stream), reps, flush, stream)
+                                                                  stream=stream), reps, flush, stream,
+                              "long_split_decode")
         nb = decode_algorithmic_bytes(c)
         res["long_split_decode"] = {"ms": med, "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm,
                                     "hbm_frac_nominal": nb / med / 1e6 / NOMINAL_HBM_GBS,
                                     "kv_bytes": nb, "partition_size": c.partition_size,
                                     "tokens_per_s": c.S / (med * 1e-3)}
+        if oracle_legs:
+            import oracle
+            res["long_split_decode"]["cpu_baseline"] = oracle_leg(
+                range(c.S), lambda si: oracle.paged_decode(c.q[si:si + 1], c.k_cache, c.v_cache,
+                                                           c.block_table[si:si + 1], c.seq_lens[si:si + 1],
+                                                           c.scale)[0],
+                nb, "GB/s", False, out, "every sequence (unsplit oracle), one oracle call each")
         del t, out, ws, c
         torch.cuda.empty_cache()
     if "c4" in names:
@@ -607,7 +702,7 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         ws = torch.empty(pa.metis_prefill_workspace_bytes(c.S, c.T, c.H, c.G), dtype=torch.uint8, device=dev)
         med, mn = _time_calls(lambda: pa.metis_paged_attn_prefill_chunk(*t, c.scale, out=out, max_seq_len=c.max_seq_len,
                                                                         workspace=ws, stream=stream), reps, flush,
-                              stream)
+                              stream, "chunked_prefill")
         cu = c.cu_q_lens.numpy()
         lens = c.seq_lens.numpy()
         flops = 0
@@ -621,7 +716,7 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         flop_ms = flops / (tc_burst * 1e9)
         byte_ms = (kv_bytes + io_bytes) / (peak_hbm * 1e6)
 
-        def sub_call(sel):
+        def sub_call(sel, name):
             # the same call over a subset of the sequences (the chunks, or the decodes)
             rows = np.concatenate([np.arange(cu[si], cu[si + 1]) for si in sel])
             sq = c.q[torch.from_numpy(rows)].contiguous().to(dev)
@@ -634,13 +729,13 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
             sm, _ = _time_calls(lambda: pa.metis_paged_attn_prefill_chunk(sq, scu, t[2], t[3], sbt, ssl, c.scale,
                                                                           out=sout, max_seq_len=c.max_seq_len,
                                                                           workspace=sws, stream=stream),
-                                reps, flush, stream)
+                                reps, flush, stream, name)
             sflops = sum(int(((lens[si] - qlen[si]) + np.arange(qlen[si]) + 1).sum()) for si in sel) * c.H * 4 * c.D
             skv = int(lens[sel].astype(np.int64).sum()) * c.G * c.D * 2 * 2
             return sm, sflops, skv
 
-        ch_ms, ch_flops, _ = sub_call(np.where(qlen > 1)[0])
-        de_ms, _, de_kv = sub_call(np.where(qlen == 1)[0])
+        ch_ms, ch_flops, _ = sub_call(np.where(qlen > 1)[0], "chunked_prefill_chunks")
+        de_ms, _, de_kv = sub_call(np.where(qlen == 1)[0], "chunked_prefill_decodes")
         res["chunked_prefill"] = {"ms": med, "TFLOP_s": tf, "tensor_frac_burst": tf / tc_burst,
                                   "tensor_frac_sustained": tf / tc_sus, "flops": flops, "tokens": c.T,
                                   "tokens_per_s": c.T / (med * 1e-3),
@@ -653,6 +748,20 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
                                   "note": "one call: 16 chunks of 512 over cached prefixes + 48 single-token decodes; "
                                           "roofline_frac = max(flop bound, byte bound) / call time; the two kinds "
                                           "also timed as calls of their own"}
+        if oracle_legs:
+            import oracle
+
+            def one_seq(si):
+                ql = int(qlen[si])
+                return oracle.paged_prefill(c.q[int(cu[si]):int(cu[si + 1])],
+                                            torch.tensor([0, ql], dtype=torch.int32), c.k_cache, c.v_cache,
+                                            c.block_table[si:si + 1], c.seq_lens[si:si + 1], c.scale)[0]
+
+            # the GPU output is in the same (sequence-major) row order
+            res["chunked_prefill"]["cpu_baseline"] = oracle_leg(
+                range(c.S), one_seq, flops, "TFLOP/s", False, out,
+                "every row of every sequence, one oracle call per sequence")
+            res["chunked_prefill"]["cpu_baseline"]["value"] /= 1e3   # GFLOP/s -> TFLOP/s
         del t, out, ws, c
         torch.cuda.empty_cache()
     if "kvw" in names:
@@ -672,10 +781,14 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         value = torch.randn(c.T, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
         kc, vc = c.k_cache.to(dev), c.v_cache.to(dev)
         med, mn = _time_calls(lambda: pa.metis_reshape_and_cache(key, value, kc, vc, slots, stream=stream), reps, flush,
-                              stream)
+                              stream, "kv_write")
         nb = 2 * 2 * c.T * c.G * c.D * 2 + c.T * 8    # K and V rows read and written, plus the slots
+        torch.cuda.synchronize()
+        blk, off = slots // c.bs, slots % c.bs
+        exact = bool(torch.equal(kc[blk, off], key) and torch.equal(vc[blk, off], value))
         res["kv_write"] = {"ms": med, "GB_s": nb / med / 1e6, "hbm_frac": nb / med / 1e6 / peak_hbm,
                            "hbm_frac_nominal": nb / med / 1e6 / NOMINAL_HBM_GBS, "bytes": nb, "tokens": c.T,
+                           "written_rows_bitwise_equal_to_inputs": exact,
                            "note": "the chunked-prefill step's new K/V rows scattered into their pages"}
         del key, value, kc, vc, slots, c
         torch.cuda.empty_cache()
@@ -744,7 +857,7 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
         ws = torch.empty(pa.metis_mla_workspace_bytes(c.S, c.H, c.max_seq_len, P), dtype=torch.uint8, device=dev)
         med, mn = _time_calls(lambda: pa.metis_mla_decode(*t, c.scale, out=out, partition_size=P,
                                                           max_seq_len=c.max_seq_len, workspace=ws, stream=stream),
-                              reps, flush, stream)
+                              reps, flush, stream, "mla_decode")
         tok = int(c.seq_lens.sum())
         flops = tok * c.H * 2 * (576 + 512)
         nb = tok * 576 * 2 + c.S * c.H * (576 + 512) * 2 + int(sum(-(-int(L) // c.bs) for L in c.seq_lens)) * 4
@@ -755,9 +868,31 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc):
                              "hbm_frac_nominal": nb / med / 1e6 / NOMINAL_HBM_GBS, "flops": flops,
                              "bytes": nb, "tokens": tok, "partition_size": P,
                              "tokens_per_s": c.S / (med * 1e-3)}
+        if oracle_legs:
+            import oracle
+            res["mla_decode"]["cpu_baseline"] = oracle_leg(
+                range(c.S), lambda si: oracle.mla_decode(c.q[si:si + 1], c.kv_cache, c.block_table[si:si + 1],
+                                                         c.seq_lens[si:si + 1], c.scale)[0],
+                flops, "TFLOP/s", False, out, "every sequence, one oracle call each")
+            res["mla_decode"]["cpu_baseline"]["value"] /= 1e3   # GFLOP/s -> TFLOP/s
         del t, out, ws, c
         torch.cuda.empty_cache()
     return res
+
+
+def run_workloads_only(args, local):
+    """Profiling aid: the --workloads list alone, timed as in the full run, printed as one JSON object."""
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    flush = L2Flush(max(2 * int(getattr(props, "L2_cache_size", 128 << 20)), 256 << 20), dev, args.flush)
+    peak, _ = load_peaks()
+    (tcb, tcs), _ = load_tc_peaks()
+    names = [w.strip() for w in args.workloads.split(",") if w.strip()]
+    res = other_workloads(names, args.workload_reps, dev, flush, torch.cuda.current_stream(dev), peak, (tcb, tcs),
+                          oracle_legs=not args.no_cpu_baseline, c3_seqs=args.c3_seqs)
+    print(json.dumps({"workloads_only": res}), flush=True)
+    return 0
 
 
 def main():
@@ -772,6 +907,10 @@ def main():
                     help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw,pfx; "
                          "empty: none)")
     ap.add_argument("--workload-reps", type=int, default=20)
+    ap.add_argument("--skip-main", action="store_true",
+                    help="profiling aid: run only the --workloads list and print it (no headline step)")
+    ap.add_argument("--c3-seqs", type=int, default=8,
+                    help="sequences of the long split-KV workload (8; fewer gives a smaller case for profiling)")
     ap.add_argument("--flush", choices=["read", "write"], default="read",
                     help="how L2 is evicted between timed steps (outside the timed events)")
     ap.add_argument("--ramp-steps", type=int, default=None,
@@ -783,6 +922,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         rc = run_reference(args, world, rank)
+    elif args.skip_main:
+        rc = run_workloads_only(args, local)
     else:
         rc = run_ours(args, world, rank, local)
     if world > 1:

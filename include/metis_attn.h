@@ -148,12 +148,14 @@ int metis_paged_attn_decode_partials(const void* q, const void* k_cache, const v
  *  - Every GPU that loads the library holds the 64 MiB until the process
  *    exits.
  *  - A split that needs more than METIS_NOALLOC_SCRATCH_BYTES
- *    (metis_decode_workspace_bytes(...) > the limit) is rejected with
- *    METIS_E_WORKSPACE and nothing is launched.  partition_size 0 needs no
- *    scratch.
- *  - The first call on a device looks up the array's device address for that
- *    device (cudaGetSymbolAddress); make that first call before any stream
- *    capture.
+ *    (metis_decode_workspace_bytes(...) > the limit, with max_seq_len clamped
+ *    to max_blocks * block_size) is rejected with METIS_E_WORKSPACE and
+ *    nothing is launched.  partition_size 0 needs no scratch.
+ *  - The first split call on a device looks up the array's device address
+ *    for that device (cudaGetSymbolAddress) and caches it with the current
+ *    CUDA context; a call under a different context (after cudaDeviceReset,
+ *    say) looks it up again.  Make the first call on a device, and the first
+ *    after a context change, before any stream capture.
  *  - Every call shares the one array.  Calls whose work overlaps on the GPU
  *    (other streams, other threads, without ordering between them) race on
  *    it and give wrong results; calls in one stream are ordered and safe.

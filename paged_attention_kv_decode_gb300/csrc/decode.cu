@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   const int s = (int)(sh / H);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = seq_lens[s];
-  const int n = L > 0 ? min((L + P - 1) / P, max_parts) : 0;
+  const int n = L > 0 ? min(L / P + (L % P != 0), max_parts) : 0;   // ceil(L / P) without overflow
   if (skip_single && n <= 1) return;  // written directly by the producing kernel
   const float* lrow = part_lse + sh * max_parts;
 
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* 
   if (sh >= (size_t)S * H) return;
   const int s = (int)(sh / H);
   const int L = seq_lens[s];
-  const int n = L > 0 ? min((L + P - 1) / P, max_parts) : 0;
+  const int n = L > 0 ? min(L / P + (L % P != 0), max_parts) : 0;   // ceil(L / P) without overflow
   if (skip_single && n <= 1) return;
   const float* lrow = part_lse + sh * max_parts;
   float M = -INFINITY;
@@ -693,8 +693,18 @@ static int launch_merge(const float* part_out, const float* part_lse, const int3
   return launch_merge_ex(part_out, part_lse, seq_lens, P, out, lse_out, S, H, D, max_parts, out_dtype, 0, st);
 }
 
+// Partitions a split call launches: ceil(max_seq_len / partition_size), in 64
+// bits (max_seq_len near INT_MAX must not overflow); 0 when unsplit.
 static size_t split_parts(int max_seq_len, int partition_size) {
-  return partition_size > 0 ? (size_t)((max_seq_len + partition_size - 1) / partition_size) : 0;
+  if (partition_size <= 0 || max_seq_len <= 0) return 0;
+  return (size_t)(((long long)max_seq_len + partition_size - 1) / partition_size);
+}
+
+// The longest sequence a call can read: max_seq_len, clamped to what a
+// block-table row addresses (max_blocks * block_size).  Partitions past it
+// would only ever be empty, so they are neither launched nor given scratch.
+static int effective_max_len(int max_seq_len, int max_blocks, int block_size) {
+  return (int)std::min<long long>((long long)max_blocks * block_size, (long long)max_seq_len);
 }
 
 // bf16 decode configuration: warps per CTA and ring depth per warp.
@@ -774,9 +784,10 @@ static int paged_decode(const void* q, const void* k_cache, const void* v_cache,
     return fail(METIS_E_SHAPE, "partition_size must be 0 or a positive multiple of 16");
   if (!(scale == scale)) return fail(METIS_E_SHAPE, "scale is NaN");
 
-  const size_t parts = split_parts(max_seq_len, partition_size);
+  const int eff_len = effective_max_len(max_seq_len, max_blocks, block_size);
+  const size_t parts = split_parts(eff_len, partition_size);
   if (parts > 0x7fffffff) return fail(METIS_E_SHAPE, "too many partitions");
-  const size_t need = metis_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_seq_len, partition_size);
+  const size_t need = metis_decode_workspace_bytes(num_seqs, num_heads, head_dim, eff_len, partition_size);
   if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return fail(METIS_E_WORKSPACE, "workspace must hold %zu bytes (256-byte aligned)", need);
 
@@ -797,7 +808,7 @@ static int paged_decode(const void* q, const void* k_cache, const void* v_cache,
   p.scale_log2 = scale * kLog2e;
   p.partition_size = partition_size;
   p.max_parts = parts ? (int)parts : 1;
-  p.cap = (int)std::min<long long>((long long)max_blocks * block_size, (long long)max_seq_len);
+  p.cap = eff_len;
   if (parts) {
     const size_t units = (size_t)num_seqs * num_heads * parts;
     p.part_out = reinterpret_cast<float*>(workspace);
@@ -887,10 +898,29 @@ constexpr size_t kNoAllocScratchBytes = METIS_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // The array's name is only a host-side stand-in in host code: its device
-// address is looked up once per device (with that device current) and cached.
+// address is looked up with cudaGetSymbolAddress (with the device current) and
+// cached per device together with the context it was looked up in.  A new
+// primary context on that device (after cudaDeviceReset, say) loads the module
+// afresh, so a context that differs from the cached one triggers a new lookup.
 constexpr int kNoAllocMaxDevices = 64;
-static void* g_noalloc_ptr[kNoAllocMaxDevices];
+struct NoAllocAddr {
+  CUcontext ctx;
+  void* ptr;
+};
+static NoAllocAddr g_noalloc[kNoAllocMaxDevices];
 static std::mutex g_noalloc_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+static CtxGetCurrentFn g_ctx_get_current = nullptr;
+static std::once_flag g_ctx_once;
+
+static void load_ctx_get_current() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+}
 
 static int noalloc_scratch_address(void** out) {
   int dev = -1;
@@ -899,14 +929,22 @@ static int noalloc_scratch_address(void** out) {
   if (dev < 0 || dev >= kNoAllocMaxDevices)
     return fail(METIS_E_UNSUPPORTED, "device ordinal %d: the static scratch serves devices 0..%d", dev,
                 kNoAllocMaxDevices - 1);
+  std::call_once(g_ctx_once, load_ctx_get_current);
+  if (!g_ctx_get_current) return fail(METIS_E_CUDA, "cuCtxGetCurrent unavailable from the driver");
+  // null before the runtime has set up this device's context on this thread
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocAddr& slot = g_noalloc[dev];
+  if (!slot.ptr || !ctx || slot.ctx != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // sets up the context if needed
     if (e != cudaSuccess) return fail(METIS_E_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = p;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return fail(METIS_E_CUDA, "no current CUDA context");
+    slot.ctx = ctx;
+    slot.ptr = p;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return METIS_OK;
 }
 
@@ -919,7 +957,10 @@ extern "C" int metis_paged_attn_decode_noalloc(const void* q, const void* k_cach
                                                int dtype, float scale, int partition_size, int max_seq_len,
                                                void* stream) {
   clear_error();
-  const size_t need = metis_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_seq_len, partition_size);
+  // scratch for the partitions the call will launch (max_seq_len clamped to
+  // what a block-table row addresses, as the decode itself does)
+  const int eff_len = max_blocks > 0 && block_size > 0 ? effective_max_len(max_seq_len, max_blocks, block_size) : 0;
+  const size_t need = metis_decode_workspace_bytes(num_seqs, num_heads, head_dim, eff_len, partition_size);
   if (need > kNoAllocScratchBytes)
     return fail(METIS_E_WORKSPACE,
                 "split-KV scratch of %zu bytes needed; the static scratch holds %zu bytes (use a larger "

@@ -151,7 +151,7 @@ struct MlaParams {
 // partitions of sequence s: the merge reads ceil(L / P) of them (at most max_parts)
 __device__ __forceinline__ int mla_parts(const MlaParams& p, int L_raw) {
   if (p.P <= 0) return 1;
-  return max(1, min((L_raw + p.P - 1) / p.P, p.max_parts));
+  return max(1, min(L_raw / p.P + (L_raw % p.P != 0), p.max_parts));   // ceil without overflow
 }
 
 __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, int4* items, int* count,
@@ -858,7 +858,7 @@ struct MlaWorkspace {
 
 static MlaWorkspace mla_workspace_layout(int S, int H, int max_seq_len, int P) {
   MlaWorkspace w{};
-  w.max_parts = P > 0 ? std::max(1, (max_seq_len + P - 1) / P) : 1;
+  w.max_parts = P > 0 ? (int)std::max<long long>(1, ((long long)max_seq_len + P - 1) / P) : 1;
   w.max_items = (size_t)S * w.max_parts;
   w.items_off = 256;
   w.part_off = align_up(w.items_off + w.max_items * sizeof(int4), 256);

@@ -165,21 +165,15 @@ def test_batched_decode_full_size():
     check_case(case, SPLIT_PARTITION)
 
 
-def test_long_split_decode_full_size_sampled():
-    """8 seqs of U[32768, 131072] tokens, 512-token partitions; the oracle checks two whole sequences."""
+def test_long_split_decode_full_size_every_output():
+    """8 seqs of U[32768, 131072] tokens, 512-token partitions merged by log-sum-exp, in the bench's launch
+    configuration: every output row and lse against the oracle (a few seconds of float64 CPU work)."""
     case = wl.config3_long_split_decode()
     out, lse = gpu_decode(case, case.partition_size)
     assert pa.metis_read_status() == 0
-    o = f64(out)
-    assert np.isfinite(o).all()
-    lens = case.seq_lens.numpy()
-    for s in (int(np.argmax(lens)), int(np.argmin(lens))):
-        sub = wl.DecodeCase(name="sub", q=case.q[s:s + 1], k_cache=case.k_cache, v_cache=case.v_cache,
-                            block_table=case.block_table[s:s + 1], seq_lens=case.seq_lens[s:s + 1],
-                            scale=case.scale)
-        ref_o, ref_l = oracle_decode(sub)
-        assert_parity(out[s:s + 1], ref_o, torch.bfloat16)
-        assert_lse(lse[s:s + 1], ref_l, torch.bfloat16)
+    ref_o, ref_l = oracle_decode(case)
+    assert_parity(out, ref_o, torch.bfloat16)
+    assert_lse(lse, ref_l, torch.bfloat16)
 
 
 # ---------------------------------------------------------------------------

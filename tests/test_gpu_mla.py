@@ -90,21 +90,15 @@ def test_empty_sequence():
         assert_parity(out, ref_o, torch.bfloat16)
 
 
-def test_mla_full_size_sampled():
-    """128 seqs, lognormal lengths (median 1024, cap 8192), 128 heads: 12 whole sequences vs the oracle."""
+def test_mla_full_size_every_output():
+    """128 seqs, lognormal lengths (median 1024, cap 8192), 128 heads, in the bench's launch configuration:
+    every output row and lse against the oracle (a few seconds of float64 CPU work)."""
     case = wl.config5_mla_decode()
     out, lse = gpu_mla(case, BENCH_MLA_PARTITION)
     assert pa.metis_read_status() == 0
-    assert np.isfinite(f64(out)).all()
-    lens = case.seq_lens.numpy()
-    order = np.argsort(lens)
-    pick = sorted(set(list(order[:4]) + list(order[-4:]) + list(order[len(order) // 2 - 2:len(order) // 2 + 2])))
-    for s in pick:
-        sub = wl.MLACase(name="sub", q=case.q[s:s + 1], kv_cache=case.kv_cache, block_table=case.block_table[s:s + 1],
-                         seq_lens=case.seq_lens[s:s + 1], scale=case.scale)
-        ref_o, ref_l = oracle_mla(sub)
-        assert_parity(out[s:s + 1], ref_o, torch.bfloat16)
-        assert_lse(lse[s:s + 1], ref_l, torch.bfloat16)
+    ref_o, ref_l = oracle_mla(case)
+    assert_parity(out, ref_o, torch.bfloat16)
+    assert_lse(lse, ref_l, torch.bfloat16)
 
 
 def test_bad_block_id_is_flagged():

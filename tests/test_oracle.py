@@ -213,6 +213,53 @@ def test_weights_sum_to_one():
     np.testing.assert_allclose(out, 1.0, rtol=0, atol=1e-15)
 
 
+def test_attention_weights_two_key_closed_form():
+    # two keys whose scaled scores differ by d: the weights are the logistic
+    # function of d, 1 / (1 + e^-d) and 1 / (1 + e^d)
+    q = np.array([0.5, -1.0, 2.0])
+    keys = np.array([[1.0, 0.0, 0.5], [0.0, 1.0, -0.5]])
+    scale = 0.7
+    d = scale * ((0.5 * 1.0 + 2.0 * 0.5) - (-1.0 * 1.0 + 2.0 * -0.5))   # scale * (z0 - z1), worked by hand
+    w = oracle.attention_weights(q, keys, scale)
+    assert w.shape == (2,)
+    assert abs(w[0] - 1.0 / (1.0 + math.exp(-d))) < 1e-15
+    assert abs(w[1] - 1.0 / (1.0 + math.exp(d))) < 1e-15
+
+
+def test_attention_weights_match_python_brute_force():
+    # sum to 1, non-negative, and equal to exp(z_t) / sum exp(z) evaluated in
+    # plain Python floats; large scores (|z| ~ 300) would overflow an
+    # unshifted exponential, so the brute force shifts by its own maximum
+    rng = np.random.default_rng(29)
+    for L, scale in ((1, 0.3), (5, 1.0), (40, 0.125), (17, 30.0)):
+        q = rng.standard_normal(8)
+        keys = rng.standard_normal((L, 8))
+        w = oracle.attention_weights(q, keys, scale)
+        z = [scale * sum(float(a) * float(b) for a, b in zip(q, k)) for k in keys]
+        m = max(z)
+        e = [math.exp(x - m) for x in z]
+        ref = [x / sum(e) for x in e]
+        assert (w >= 0).all()
+        assert abs(w.sum() - 1.0) < 1e-14
+        np.testing.assert_allclose(w, ref, rtol=1e-13, atol=1e-300)
+
+
+def test_attention_weights_are_the_decode_weights():
+    # the weighted sum of the value rows with these weights is the decode output
+    # (a dropped scale or a transposed product in either would break it)
+    rng = np.random.default_rng(31)
+    L, bs, D = 45, 16, 16
+    kc = rng.standard_normal((3, bs, 1, D))
+    vc = rng.standard_normal((3, bs, 1, D))
+    q = rng.standard_normal((1, 1, D))
+    table = np.array([[2, 0, 1]], dtype=np.int32)
+    out, _ = oracle.paged_decode(q, kc, vc, table, np.array([L]), 0.4)
+    K = np.stack([kc[table[0, t // bs], t % bs, 0] for t in range(L)])
+    V = np.stack([vc[table[0, t // bs], t % bs, 0] for t in range(L)])
+    w = oracle.attention_weights(q[0, 0], K, 0.4)
+    np.testing.assert_allclose(w @ V, out[0, 0], rtol=1e-13, atol=1e-14)
+
+
 def test_dominant_key_selects_its_value():
     rng = np.random.default_rng(13)
     kc = rng.standard_normal((2, 16, 1, 8)) * 0.01
