@@ -60,7 +60,7 @@ METRIC = "decode KV GB/s (% of HBM peak) and tokens/s; prefill TFLOP/s, 1 GB300"
 WORKLOAD = ("batched paged decode, bf16 KV: 64 seqs, seq_lens U[512,4096], 32 q / 8 kv heads, head_dim 128, "
             "block_size 16, block_table a random permutation of the pool")
 PARTITION = 0      # unsplit: one CTA per (sequence, kv head), longest sequences first (no merge)
-MLA_PARTITION = 3072
+MLA_PARTITION = 2048
 E2E_LAYERS = 4      # distinct layer caches the pipelined end-to-end leg cycles through
 NOMINAL_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth; fractions are reported against it and the measured peak
 FALLBACK_HBM_GBS = 6800.0

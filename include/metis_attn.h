@@ -230,7 +230,7 @@ size_t metis_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads
  *   q          [num_seqs, num_heads, d_latent + d_rope] bf16
  *   kv_cache   [num_blocks, block_size, d_latent + d_rope] bf16
  *   block_table, seq_lens   as for metis_paged_attn_decode
- *   out        [num_seqs, num_heads, d_latent] bf16 (written)
+ *   out        [num_seqs, num_heads, d_latent] bf16 (written), 32-byte aligned
  *   lse_out    fp32 [num_seqs, num_heads] or NULL
  *   partition_size  0: one pass per sequence; > 0 (a multiple of 32): tokens
  *              are split into partitions of that size, computed in parallel and
@@ -241,8 +241,9 @@ size_t metis_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads
  *
  * Supported: d_latent 512, d_rope 64; num_heads a multiple of 128, or a
  * multiple of 16 below 128; block_size 16, 32 or 64.  Tensor cores: bf16
- * operands, fp32 accumulation.  Each work item runs on a cluster of two CTAs
- * (two SMs) that split the key dimensions and the output columns.
+ * operands, fp32 accumulation.  Persistent clusters of two CTAs (two SMs), one
+ * per SM pair, split the key dimensions and the output columns of each work
+ * item (a sequence, or a partition of one) and walk their share of the items.
  */
 int metis_mla_decode(const void* q, const void* kv_cache,
                      const int32_t* block_table, const int32_t* seq_lens,

@@ -55,6 +55,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// 16-byte store into a peer CTA's shared memory (address from dsmem_map).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Asynchronous 16-byte store into a peer CTA's shared memory that signals
+// complete_tx(16) on the peer's mbarrier `cluster_bar_addr` when it lands (the
+// receiver arms the barrier with expect_tx for the bytes it awaits; a thread
+// that sees the phase complete sees the data).  The sender does not wait.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cluster_bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar_addr)
+               : "memory");
+}
+
+// Arrive on an mbarrier of another CTA with release semantics at cluster scope:
+// this thread's earlier stores into that CTA's shared memory are visible to a
+// thread that observes the phase completing with an acquire.cluster wait.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cluster_bar_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr) : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -493,15 +493,26 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
 constexpr int kMergeThreads = 128;
 constexpr int kMergeMaxD = 512;
 
+// One CTA per (sequence, head) when there are many partitions.  The partition
+// weights exp(lse_i - max) are computed once into shared memory; then each warp
+// sums every kMergeWarps-th partition, kMergeUnroll partitions per step so that
+// that many row loads per lane are in flight at once (the sum is bound by memory
+// latency, not by bandwidth, at one row per warp).
+constexpr int kMergeWarps = 8;
+constexpr int kMergeUnroll = 4;
+constexpr int kMergeCache = 2048;   // partitions whose weights are cached (beyond: recomputed per row)
+
 template <typename OutT>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ part_out,
-                                                              const float* __restrict__ part_lse,
-                                                              const int32_t* __restrict__ seq_lens, int P,
-                                                              OutT* __restrict__ out, float* __restrict__ lse_out,
-                                                              int H, int D, int max_parts, int skip_single) {
-  constexpr int NWARP = kMergeThreads / 32;
-  __shared__ float red[NWARP];
-  __shared__ float4 acc_s[NWARP][kMergeMaxD / 4];
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const float* __restrict__ part_out,
+                                                                 const float* __restrict__ part_lse,
+                                                                 const int32_t* __restrict__ seq_lens, int P,
+                                                                 OutT* __restrict__ out, float* __restrict__ lse_out,
+                                                                 int H, int D, int max_parts, int skip_single) {
+  constexpr int NT = kMergeWarps * 32;
+  constexpr int NJ = kMergeMaxD / 128;   // float4 columns per lane
+  __shared__ float red[kMergeWarps];
+  __shared__ float wts[kMergeCache];
+  __shared__ float4 acc_s[kMergeWarps][kMergeMaxD / 4];
   pdl_wait();  // the partials of the kernel before this one are complete and visible
   const size_t sh = blockIdx.x;
   const int s = (int)(sh / H);
@@ -513,65 +524,83 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
 
   // max of the partition lse values (natural log)
   float M = -INFINITY;
-  for (int i = threadIdx.x; i < n; i += kMergeThreads) M = fmaxf(M, lrow[i]);
+  for (int i = threadIdx.x; i < n; i += NT) M = fmaxf(M, lrow[i]);
   M = warp_max_xor(M, 1);
   if (lane == 0) red[warp] = M;
   __syncthreads();
   M = red[0];
 #pragma unroll
-  for (int w = 1; w < NWARP; ++w) M = fmaxf(M, red[w]);
+  for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
   const bool empty = !(M > -INFINITY);
   const float M2 = M * kLog2e;
   __syncthreads();
 
+  // weights (0 for an empty partition, whose row is never read) and their sum
   float W = 0.f;
   if (!empty)
-    for (int i = threadIdx.x; i < n; i += kMergeThreads) {
+    for (int i = threadIdx.x; i < n; i += NT) {
       const float x = lrow[i];
-      if (x > -INFINITY) W += exp2_approx(fmaf(x, kLog2e, -M2));
+      const float w = x > -INFINITY ? exp2_approx(fmaf(x, kLog2e, -M2)) : 0.f;
+      if (i < kMergeCache) wts[i] = w;
+      W += w;
     }
   W = warp_sum_xor(W, 1);
   if (lane == 0) red[warp] = W;
   __syncthreads();
   W = 0.f;
 #pragma unroll
-  for (int w = 0; w < NWARP; ++w) W += red[w];
+  for (int w = 0; w < kMergeWarps; ++w) W += red[w];
 
-  // warp w sums partitions w, w + NWARP, ...; lane owns float4 columns lane, lane + 32, ...
+  // warp w sums partitions w, w + kMergeWarps, ...; lane owns float4 columns lane, lane + 32, ...
   const int nq = D / 4;
-  float4 acc[kMergeMaxD / 128];
+  float4 acc[NJ];
 #pragma unroll
-  for (int j = 0; j < kMergeMaxD / 128; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < NJ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!empty) {
     const float4* prow = reinterpret_cast<const float4*>(part_out + sh * max_parts * D);
-    for (int i = warp; i < n; i += NWARP) {
-      const float x = lrow[i];
-      if (!(x > -INFINITY)) continue;
-      const float w = exp2_approx(fmaf(x, kLog2e, -M2));
+    for (int i0 = warp; i0 < n; i0 += kMergeWarps * kMergeUnroll) {
+      float w[kMergeUnroll];
+      float4 v[kMergeUnroll][NJ];
 #pragma unroll
-      for (int j = 0; j < kMergeMaxD / 128; ++j) {
-        const int c = lane + 32 * j;
-        if (c < nq) {
-          const float4 v = __ldg(prow + (size_t)i * nq + c);
-          acc[j].x = fmaf(w, v.x, acc[j].x);
-          acc[j].y = fmaf(w, v.y, acc[j].y);
-          acc[j].z = fmaf(w, v.z, acc[j].z);
-          acc[j].w = fmaf(w, v.w, acc[j].w);
+      for (int k = 0; k < kMergeUnroll; ++k) {
+        const int i = i0 + k * kMergeWarps;
+        w[k] = 0.f;
+        if (i < n) {
+          if (i < kMergeCache) {
+            w[k] = wts[i];
+          } else {
+            const float x = lrow[i];
+            w[k] = x > -INFINITY ? exp2_approx(fmaf(x, kLog2e, -M2)) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int c = lane + 32 * j;
+          v[k][j] = (w[k] != 0.f && c < nq) ? __ldg(prow + (size_t)i * nq + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+#pragma unroll
+      for (int k = 0; k < kMergeUnroll; ++k)
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          acc[j].x = fmaf(w[k], v[k][j].x, acc[j].x);
+          acc[j].y = fmaf(w[k], v[k][j].y, acc[j].y);
+          acc[j].z = fmaf(w[k], v[k][j].z, acc[j].z);
+          acc[j].w = fmaf(w[k], v[k][j].w, acc[j].w);
+        }
     }
   }
 #pragma unroll
-  for (int j = 0; j < kMergeMaxD / 128; ++j) {
+  for (int j = 0; j < NJ; ++j) {
     const int c = lane + 32 * j;
     if (c < nq) acc_s[warp][c] = acc[j];
   }
   __syncthreads();
   const float inv = empty ? 0.f : 1.0f / W;
-  for (int c = threadIdx.x; c < nq; c += kMergeThreads) {
+  for (int c = threadIdx.x; c < nq; c += NT) {
     float4 t = acc_s[0][c];
 #pragma unroll
-    for (int w = 1; w < NWARP; ++w) {
+    for (int w = 1; w < kMergeWarps; ++w) {
       t.x += acc_s[w][c].x;
       t.y += acc_s[w][c].y;
       t.z += acc_s[w][c].z;
@@ -681,10 +710,10 @@ int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t*
   }
   const dim3 grid((unsigned)pairs);
   if (out_dtype == METIS_BF16)
-    return launch_dependent(merge_kernel<__nv_bfloat16>, grid, dim3(kMergeThreads), 0, st, "merge kernel launch",
+    return launch_dependent(merge_kernel<__nv_bfloat16>, grid, dim3(kMergeWarps * 32), 0, st, "merge kernel launch",
                             part_out, part_lse, seq_lens, P, reinterpret_cast<__nv_bfloat16*>(out), lse_out, H, D,
                             max_parts, skip_single);
-  return launch_dependent(merge_kernel<float>, grid, dim3(kMergeThreads), 0, st, "merge kernel launch", part_out,
+  return launch_dependent(merge_kernel<float>, grid, dim3(kMergeWarps * 32), 0, st, "merge kernel launch", part_out,
                           part_lse, seq_lens, P, reinterpret_cast<float*>(out), lse_out, H, D, max_parts, skip_single);
 }
 

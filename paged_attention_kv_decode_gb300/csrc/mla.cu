@@ -9,47 +9,55 @@
 // arrive already in latent space (the absorbed up-projection is upstream).
 //
 // Decomposition.  A (sequence, partition) is computed by a CLUSTER OF TWO CTAs
-// (two SMs); nothing is computed twice and every latent byte is read once:
+// (two SMs), because one SM cannot hold the 128 x 512 fp32 output (all of TMEM)
+// next to the scores and the queries:
 //   * scores: CTA r owns the key dimensions D_r = [256 r, 256 r + 256) of the
 //     latent part plus [512 + 32 r, 512 + 32 r + 32) of the rope part and
 //     computes the partial S_r = Q[:, D_r] K[:, D_r]^T for all 128 heads;
-//   * softmax: CTA r owns heads [64 r, 64 r + 64).  It sends its partial scores
-//     of the other 64 heads to the peer and receives the peer's partial of its
-//     own heads (fp32, through distributed shared memory), runs the online
-//     softmax of its heads, and sends P of its heads (bf16) plus their rescale
-//     factors back, so both CTAs hold P of all heads;
+//   * ONE exchange per 64-token unit: each CTA stores its partial scores of
+//     all heads straight into the peer's shared memory (asynchronous
+//     distributed-shared-memory stores that count their bytes on the peer's
+//     barrier, which the peer armed with the 32 KB it awaits), so both
+//     CTAs form the full S = S_0 + S_1 (fp32 addition commutes: both get the
+//     same bits) and both run the softmax of every head -- no probabilities
+//     travel back;
 //   * output: CTA r owns output columns [256 r, 256 r + 256) (O_r in TMEM), whose
 //     values are exactly the latent columns it already loads for its keys.
 //
-// Granularity.  A UMMA costs at least ~46 cycles whatever its N, so the scores
-// are computed for 64-token tiles (N = 64); the exchange, the softmax and P V run
-// on 32-token units, two per tile.  Per CTA and unit that is 18 KB of latent
-// (four 128-byte-swizzled 64-column blocks plus one 64-byte-swizzled 32-column
-// rope half block), streamed through an 8-unit TMA ring laid out block-major so
-// that the two units of a tile form one 64-row operand per block.
+// Online softmax with a lagged reference.  Two sets of row warps take the even
+// and the odd units.  Unit u exponentiates against a reference c_u (log2
+// domain): R_{u-2} = max(c_0 .. c_{u-2}), the reference O holds after unit
+// u - 2, kept as long as the unit's own maximum stays within 2^8 of it, else the
+// unit's maximum.  So P <= 2^8 always, every choice depends on the data alone
+// (results are bitwise reproducible), and a set needs from the other set only
+// R_{u-3}, which that set publishes as it starts unit u - 1, a unit ahead of
+// use.  Each unit hands its
+// P (bf16, shared memory), c and row sum to four rescale warps, which replay
+// the units in order against O's reference C: c > C rescales O in TMEM by
+// 2^(C - c) (after the previous P V completes); c < C scales the unit's P rows
+// by 2^(c - C) instead (never O up, which could overflow); c = C costs nothing.
 //
-// TMEM (512 columns): O_r 256 | S 2 x 64 | the latent part of Q_r as bf16 pairs,
-// 128 (the A operand of the score UMMA).  The rope part of Q_r and the P tiles
-// (the A operand of P V) sit in shared memory, so a score buffer is free as soon
-// as it has been read and the next scores never wait for P V.
+// Per 64-token unit and CTA: 36 KB of latent through a 4-stage TMA ring (four
+// 128-byte-swizzled 64-column blocks and one 64-byte-swizzled 32-column rope
+// block); the score UMMA is M 128 x N 64 x K 288 (Q_r's latent part from TMEM,
+// its rope part from shared memory); P V is M 128 x N 256 x K 64.  The unit's
+// 32 KB exchange slot first receives the peer's partial scores, then holds P
+// (the peer writes the slot again only after P V of the unit completed, which
+// the UMMA warp signals to it with a multicast commit).  The slot is laid out
+// per row warp: warp w's 32 heads own bytes [8 KB w, 8 KB (w + 1)), the scores
+// as [16-byte chunk][lane] (so one warp-wide store or load is 512 contiguous
+// bytes, also across the cluster), and P's 128-byte-swizzled rows in 8-row
+// groups 2 KB apart, so the P rows of warp w fall inside warp w's own scores:
+// a warp overwrites what it has just read and needs no other warp.
 //
-// Head order.  TMEM lane L = 32 q + 16 g + i (quarter q, half g, i < 16) holds
-// head 64 g + 16 q + i of the head tile, so every lane quarter -- and with it
-// every SM sub-partition, since warp w may only touch quarter w % 4 -- holds 16
-// heads of each CTA: the softmax work is spread over all four sub-partitions.
+// TMEM (512 columns): O_r 256 | S 2 x 64 | Q_r's latent part as bf16 pairs 128.
 //
 // Warps:
-//   0-3   row warps (quarter = warp): stage the partial scores of the peer's 16
-//         heads of the quarter one unit ahead; softmax of its own 16 heads with
-//         two lanes per head (lane i and i ^ 16, 16 tokens each; row maxima and
-//         sums combined by shuffles); write P and the rescale factors; epilogue
-//   4-7   rescale warps (quarter = warp - 4): once P of a unit is complete in
-//         both CTAs, apply its rescale factors (own and peer heads) to O in TMEM
-//   8     TMA producer          9    TMEM allocation + UMMA issue
-//   10    score exchange: bulk copy staged partials to the peer, credit the peer
-//         once a receive buffer has been read
-//   11    P exchange: bulk copy P rows of own heads (+ factors) to the peer,
-//         credit the peer once P V has released a P slot; final row statistics
+//   0-3, 4-7  row warps, set 0 (even units) and set 1 (odd units); thread =
+//             head row = TMEM lane (warp w may only touch lanes 32 (w % 4) ..)
+//   8-11      rescale warps: load Q_r, replay the units' references in order,
+//             epilogue (O / l, lse)
+//   12        TMA producer      13   TMEM allocation + score UMMAs      14   P V UMMAs      15 idle
 //
 // A schedule kernel lists the (sequence, partition) work items heaviest first.
 // A sequence with one partition writes its output directly; longer ones write
@@ -71,68 +79,56 @@ __device__ unsigned int g_status_mla = 0;
 constexpr int kMlaDq = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaHalf = 256;       // output columns (and latent key columns) per CTA
-constexpr int kMlaUnit = 32;        // tokens per exchange / softmax / P V unit and per ring stage
-constexpr int kMlaTile = 64;        // tokens per score UMMA (two units)
+constexpr int kMlaUnit = 64;        // tokens per unit: one score tile (UMMA N), exchange, softmax step and P V
+constexpr int kMlaAlign = 32;       // partitions start on multiples of this many tokens (TMA boxes never cross pages)
 constexpr int kMlaRows = 128;       // heads per head tile (the UMMA M)
-constexpr int kMlaOwn = 64;         // heads whose softmax a CTA runs
 constexpr int kMlaThreads = 512;    // 16 warps
-constexpr int kMlaRegsRow = 160;    // warpgroups 0 and 3: the two row-warp sets
-constexpr int kMlaRegsLow = 96;     // warpgroups 1 and 2: staging/rescale, TMA, UMMA, exchanges
+constexpr int kMlaRegsRow = 144;    // warpgroups 0 and 1: the two row-warp sets
+constexpr int kMlaRegsLow = 112;    // warpgroups 2 and 3: rescale, TMA, UMMA
 static_assert(128 * (2 * kMlaRegsRow + 2 * kMlaRegsLow) <= 65536, "register split exceeds the register file");
 constexpr int kMlaTmemCols = 512;
 constexpr int kMlaSortMax = 2048;
-#ifndef METIS_MLA_STAGES
-#define METIS_MLA_STAGES 8
-#define METIS_MLA_NX 2
-#define METIS_MLA_NP 3
-#endif
-constexpr int kMlaStages = METIS_MLA_STAGES;  // ring stages of one unit (even: a tile is two adjacent stages)
-constexpr int kMlaNX = METIS_MLA_NX;          // partial-score exchange slots (even: each row set uses every other)
-constexpr int kMlaNP = METIS_MLA_NP;          // P tile slots
-static_assert(kMlaStages % 2 == 0 && kMlaNX % 2 == 0, "stage and exchange-slot counts must be even");
+constexpr int kMlaStages = 4;       // TMA ring stages (one unit each)
+constexpr float kMlaSlack = 8.0f;   // a unit keeps a published reference while its maximum is within 2^8 of it
+constexpr int kMlaWorkCache = 256;  // works per cluster kept in shared memory (beyond: read from the list)
 constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
-constexpr uint32_t kTmS = 256;      // 2 x 64 columns: partial scores of a tile
+constexpr uint32_t kTmS = 256;      // 2 x 64 columns: partial scores of the units of set 0 / set 1
 constexpr uint32_t kTmQ = 384;      // 128 columns: latent part of Q_r as bf16 pairs
 
 struct MlaShape {
-  static constexpr int kBlk = kMlaUnit * 128;             // one unit of one 64-column block (128-byte swizzle)
-  static constexpr int kRopeU = kMlaUnit * 64;            // one unit of the rope half block (64-byte swizzle)
-  static constexpr int kXBuf = kMlaOwn * kMlaUnit * 4;    // partial scores of 64 heads x one unit, fp32
-  static constexpr int kPBuf = kMlaRows * kMlaUnit * 2;   // P of 128 lanes x one unit, bf16, 64-byte swizzle
-  static constexpr int kKv = 0;                           // block b of stage s at kKv + (b * kMlaStages + s) * kBlk
-  static constexpr int kRope = kKv + 4 * kMlaStages * kBlk;  // stage s at kRope + s * kRopeU
-  static constexpr int kQr = kRope + kMlaStages * kRopeU;    // rope part of Q_r: 128 lanes x 64 B, 64-byte swizzle
-  static constexpr int kStg = kQr + kMlaRows * 64;        // kMlaNX staging buffers (copied to the peer)
-  static constexpr int kRx = kStg + kMlaNX * kXBuf;       // kMlaNX receive buffers (written by the peer)
-  static constexpr int kP = kRx + kMlaNX * kXBuf;         // kMlaNP P tiles
-  static constexpr int kAlpha = kP + kMlaNP * kPBuf;      // kMlaNP x 128 rescale factors (head order)
-  static constexpr int kStat = kAlpha + kMlaNP * kMlaRows * 4;  // 128 x {m, l} (head order)
-  static constexpr int kHand = kStat + kMlaRows * 8;       // 2 sets x 128 running maxima + 128 row-sum shares
-  static constexpr int kBars = kHand + 3 * kMlaRows * 4;
-  static constexpr int kSmem = kBars + 1024 + 1024;       // barriers + alignment slack
+  static constexpr int kBlk = kMlaUnit * 128;             // one 64-column block of a unit (128-byte rows)
+  static constexpr int kStage = 4 * kBlk;                 // the unit's latent columns of this CTA
+  static constexpr int kRopeU = kMlaUnit * 64;            // the unit's rope half block (64-byte rows)
+  static constexpr int kSlotB = kMlaRows * kMlaUnit * 4;  // exchange slot: fp32 partial scores, later bf16 P
+  static constexpr int kWarpB = kSlotB / 4;               // a row warp's part of the slot
+  static constexpr int kPGroup = 2048;                    // P: bytes between 8-row groups
+  static constexpr int kKv = 0;                           // stage s at kKv + s * kStage, block b at + b * kBlk
+  static constexpr int kRope = kKv + kMlaStages * kStage; // stage s at kRope + s * kRopeU
+  static constexpr int kSlot = kRope + kMlaStages * kRopeU;  // slot k (units of set k) at kSlot + k * kSlotB
+  static constexpr int kQr = kSlot + 2 * kSlotB;          // rope part of Q_r: 128 rows x 64 B, 64-byte swizzle
+  static constexpr int kTag = kQr + kMlaRows * 64;        // per slot: 128 references c, 128 row sums l
+  static constexpr int kRef = kTag + 2 * 2 * kMlaRows * 4;  // per set: R_w of its last unit w, 128 heads
+  static constexpr int kWorks = kRef + 2 * kMlaRows * 4;   // the cluster's work list: int4 {s, part, ht, L_raw}
+  static constexpr int kBars = kWorks + kMlaWorkCache * 16;
+  static constexpr int kSmem = kBars + 512 + 1024;        // barriers + alignment slack
 };
 static_assert(MlaShape::kSmem <= 227 * 1024, "MLA shared memory exceeds the per-CTA limit");
+static_assert(MlaShape::kSlot % 1024 == 0 && MlaShape::kSlotB % 1024 == 0, "P tiles must sit on 1024-byte atoms");
 
 // mbarrier layout (indices into the barrier area) and arrival counts
 struct MlaBar {
   static constexpr int kKvFull = 0, kKvEmpty = kKvFull + kMlaStages, kSFull = kKvEmpty + kMlaStages,
-                       kPvDone = kSFull + 2, kStaged = kPvDone + 4, kRxFull = kStaged + kMlaNX,
-                       kRxRead = kRxFull + kMlaNX, kTxOk = kRxRead + kMlaNX, kPLocal = kTxOk + kMlaNX,
-                       kPRemote = kPLocal + kMlaNP, kPRelay = kPRemote + kMlaNP, kPslotOk = kPRelay + kMlaNP,
-                       kQFull = kPslotOk + kMlaNP, kStatLocal = kQFull + 1, kStatFull = kStatLocal + 1,
-                       kDrain = kStatFull + 1, kSFree = kDrain + 1, kHand = kSFree + 2, kFin = kHand + 8,
-                       kCount = kFin + 1;
+                       kSFree = kSFull + 2, kRxFull = kSFree + 2, kTxOk = kRxFull + 2,
+                       kPFull = kTxOk + 2, kPGo = kPFull + 2, kPvDone = kPGo + 2, kRefFull = kPvDone + 2,
+                       kQFull = kRefFull + 2, kOFree = kQFull + 1, kDrain = kOFree + 1, kCount = kDrain + 2;
   __host__ __device__ static constexpr int arrivals(int i) {
-    return (i >= kSFree && i < kSFree + 2) ? 256
-           : (i >= kHand && i < kHand + 8) ? 32
-           : ((i >= kStaged && i < kStaged + kMlaNX) || (i >= kRxRead && i < kRxRead + kMlaNX) ||
-              (i >= kPLocal && i < kPLocal + kMlaNP) || (i >= kPRelay && i < kPRelay + kMlaNP) || i == kQFull ||
-              i == kStatLocal || i == kFin)
+    return ((i >= kSFree && i < kSFree + 2) || (i >= kPFull && i < kPFull + 2) || (i >= kPGo && i < kPGo + 2) ||
+            (i >= kRefFull && i < kRefFull + 2) || i == kQFull || i == kOFree)
                ? 128
                : 1;
   }
 };
-static_assert((MlaBar::kCount + 2) * 8 <= 1024, "MLA barrier area");
+static_assert((MlaBar::kCount + 3) * 8 <= 512, "MLA barrier area");
 
 struct MlaParams {
   const uint4* q;   // [S, H, 576] bf16, read as 16-byte chunks
@@ -145,6 +141,7 @@ struct MlaParams {
   const int4* items;
   const int* item_count;
   int S, H, hrows, head_tiles, bs, max_blocks, num_blocks, cap, P, max_parts;
+  int box_rows;     // rows per TMA box (a divisor of the unit that never crosses a page)
   float scale_log2;
 };
 
@@ -205,6 +202,40 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, i
   if (tid == 0) *count = total;
 }
 
+// One (item, head tile) of a cluster's work: the tokens [t0, t1) of sequence s.
+struct MlaWork {
+  int s, part, ht, L_raw, t0, t1, n_units;
+  bool direct;
+};
+
+// Position in the heaviest-first list of the r-th work of cluster c of G: the
+// positions c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (a snake over the list), which
+// balances the lognormal lengths nearly as well as greedy longest-first
+// assignment and needs no communication.
+__device__ __forceinline__ long long mla_work_pos(int c, int G, int r) {
+  return (long long)r * G + ((r & 1) ? G - 1 - c : c);
+}
+
+// {s, part, ht, L_raw} of list position pos (global reads)
+__device__ __forceinline__ int4 mla_work_raw(const MlaParams& p, long long pos) {
+  const int4 it = p.items[(int)(pos / p.head_tiles)];
+  return make_int4(it.x, it.y, (int)(pos % p.head_tiles), p.seq_lens[it.x]);
+}
+
+__device__ __forceinline__ MlaWork mla_work_decode(const MlaParams& p, int4 raw) {
+  MlaWork w;
+  w.s = raw.x;
+  w.part = raw.y;
+  w.ht = raw.z;
+  w.L_raw = raw.w;
+  const int L = max(0, min(w.L_raw, p.cap));
+  w.direct = mla_parts(p, w.L_raw) == 1;
+  w.t0 = p.P > 0 ? w.part * p.P : 0;
+  w.t1 = p.P > 0 ? min(L, w.t0 + p.P) : L;
+  w.n_units = w.t1 > w.t0 ? (w.t1 - w.t0 + kMlaUnit - 1) / kMlaUnit : 0;
+  return w;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKVh,
                       const MlaParams p) {
@@ -216,87 +247,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   uint8_t* smem = smem_raw + slack;
   uint8_t* sKV = smem + Sh::kKv;
   uint8_t* sRope = smem + Sh::kRope;
+  uint8_t* sSlot = smem + Sh::kSlot;
   uint8_t* sQr = smem + Sh::kQr;
-  uint8_t* sStg = smem + Sh::kStg;
-  uint8_t* sRx = smem + Sh::kRx;
-  uint8_t* sP = smem + Sh::kP;
-  float* sAlpha = reinterpret_cast<float*>(smem + Sh::kAlpha);
-  float* sStat = reinterpret_cast<float*>(smem + Sh::kStat);
+  float* sTagC = reinterpret_cast<float*>(smem + Sh::kTag);          // [2][128]
+  float* sTagL = sTagC + 2 * kMlaRows;                                // [2][128]
+  float* sRef = reinterpret_cast<float*>(smem + Sh::kRef);           // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBars);
-  uint64_t* kv_full = bars + MlaBar::kKvFull;       // [kMlaStages]
-  uint64_t* kv_empty = bars + MlaBar::kKvEmpty;     // [kMlaStages]
-  uint64_t* s_full = bars + MlaBar::kSFull;         // [2] partial scores of tile j in S[j & 1]
-  uint64_t* pv_done = bars + MlaBar::kPvDone;       // [4] P V of unit u completed, on u % 4
-  uint64_t* staged = bars + MlaBar::kStaged;        // [kMlaNX] partial scores of the peer's heads staged (128 arrivals)
-  uint64_t* rx_full = bars + MlaBar::kRxFull;       // [kMlaNX] the peer's partial of own heads landed (armed with expect_tx)
-  uint64_t* rx_read = bars + MlaBar::kRxRead;       // [kMlaNX] a receive buffer has been read (128 arrivals)
-  uint64_t* tx_ok = bars + MlaBar::kTxOk;           // [kMlaNX] credit from the peer: it has read what we sent (remote)
-  uint64_t* p_local = bars + MlaBar::kPLocal;       // [kMlaNP] P of own heads + factors written (128 arrivals)
-  uint64_t* p_remote = bars + MlaBar::kPRemote;     // [kMlaNP] P of the peer's heads + factors landed (armed with expect_tx)
-  uint64_t* p_relay = bars + MlaBar::kPRelay;       // [kMlaNP] O rescaled for the unit, P complete (128 arrivals)
-  uint64_t* pslot_ok = bars + MlaBar::kPslotOk;     // [kMlaNP] credit from the peer: its P slot is free (remote)
-  uint64_t* q_full = bars + MlaBar::kQFull;         // Q_r in TMEM / shared memory (128 arrivals)
-  uint64_t* stat_local = bars + MlaBar::kStatLocal; // final statistics of own heads written (128 arrivals)
-  uint64_t* stat_full = bars + MlaBar::kStatFull;   // final statistics of the peer's heads landed (armed with expect_tx)
-  uint64_t* drain = bars + MlaBar::kDrain;
-  uint64_t* s_free = bars + MlaBar::kSFree;         // [2] both units of tile j have been read from S[j & 1] (256 arrivals)
-  uint64_t* hand = bars + MlaBar::kHand;            // [2 sets][4 quarters] running max after a unit of that set (32 arrivals)
-  uint64_t* fin = bars + MlaBar::kFin;              // set 1's share of the row sums handed to set 0 (128 arrivals)
+  uint64_t* kv_full = bars + MlaBar::kKvFull;    // [stages] TMA landed
+  uint64_t* kv_empty = bars + MlaBar::kKvEmpty;  // [stages] P V of the stage's unit completed
+  uint64_t* s_full = bars + MlaBar::kSFull;      // [2] partial scores of unit g in S[g & 1]
+  uint64_t* s_free = bars + MlaBar::kSFree;      // [2] S[k] has been read (128 arrivals)
+  uint64_t* rx_full = bars + MlaBar::kRxFull;    // [2] the peer's partial scores landed in slot k (32 KB of tx)
+  uint64_t* tx_ok = bars + MlaBar::kTxOk;        // [2] the peer's slot k is free again (peer's multicast commit)
+  uint64_t* p_full = bars + MlaBar::kPFull;      // [2] P, references and row sums of a unit written (128)
+  uint64_t* p_go = bars + MlaBar::kPGo;          // [2] the unit's references replayed: P V may run (128)
+  uint64_t* pv_done = bars + MlaBar::kPvDone;    // [2] P V of unit g completed, on g & 1
+  uint64_t* ref_full = bars + MlaBar::kRefFull;  // [2] set k published R of its unit in sRef[k] (128 arrivals)
+  uint64_t* q_full = bars + MlaBar::kQFull;      // Q_r of the next work in TMEM and shared memory (128)
+  uint64_t* o_free = bars + MlaBar::kOFree;      // O of a work read out: the next work may overwrite it (128)
+  uint64_t* drain = bars + MlaBar::kDrain;        // [2] after an abort: the UMMAs each issuer warp issued completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + MlaBar::kCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + MlaBar::kCount + 1);
-  float* sHand = reinterpret_cast<float*>(smem + Sh::kHand);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
   const uint32_t peer = rank ^ 1u;
-  const int rest = blockIdx.x >> 1;
-  const int ht = rest % p.head_tiles;
-  const int item_idx = rest / p.head_tiles;
-  if (item_idx >= *p.item_count) return;  // both CTAs of the cluster take the same branch
-  const int4 it = p.items[item_idx];
-  const int s = it.x, part = it.y;
-  const int L_raw = p.seq_lens[s];
-  int L = L_raw;
-  if (L > p.cap) {
-    if (threadIdx.x == 0 && rank == 0 && ht == 0 && part == 0) atomicOr(&g_status_mla, METIS_STATUS_SEQ_TOO_LONG);
-    L = p.cap;
+  const int cl = blockIdx.x >> 1, G = gridDim.x >> 1;
+  const int n_work = *p.item_count * p.head_tiles;
+  if (cl >= n_work) return;  // both CTAs of the cluster take the same branch
+  // The cluster's works, cached in shared memory (every role walks the same list;
+  // the units of all works are numbered g = 0, 1, ...).
+  int4* sWorks = reinterpret_cast<int4*>(smem + Sh::kWorks);
+  int* sCount = reinterpret_cast<int*>(bars + MlaBar::kCount + 2);
+  if (threadIdx.x == 0) sCount[0] = 0;
+  __syncthreads();
+  int my_units = 0;
+  for (int r = threadIdx.x; r < kMlaWorkCache; r += kMlaThreads) {
+    const long long pos = mla_work_pos(cl, G, r);
+    if (pos >= n_work) break;
+    const int4 raw = mla_work_raw(p, pos);
+    sWorks[r] = raw;
+    my_units += mla_work_decode(p, raw).n_units;
   }
-  if (L < 0) L = 0;
-  const bool direct = mla_parts(p, L_raw) == 1;
-  const int t0 = p.P > 0 ? part * p.P : 0;
-  const int t1 = p.P > 0 ? min(L, t0 + p.P) : L;
-  const int h0 = ht * kMlaRows;
-  if (t1 <= t0) {
-    // nothing readable: an empty sequence gets 0 / -inf, an empty partition lse = -inf
-    for (int r = threadIdx.x; r < kMlaRows; r += kMlaThreads) {
-      const int head = h0 + r;
-      if (head >= p.H) continue;
-      const size_t sh = (size_t)s * p.H + head;
-      if (direct) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf;
-        for (int c = 0; c < kMlaHalf; ++c) o[c] = __float2bfloat16(0.f);
-        if (rank == 0 && p.lse_out) p.lse_out[sh] = -INFINITY;
-      } else if (rank == 0) {
-        p.part_lse[sh * p.max_parts + part] = -INFINITY;
-      }
-    }
-    return;
+  atomicAdd(sCount, my_units);
+  __syncthreads();
+  int g_total = sCount[0];
+  for (int r = kMlaWorkCache;; ++r) {  // works past the cache (very long lists only)
+    const long long pos = mla_work_pos(cl, G, r);
+    if (pos >= n_work) break;
+    g_total += mla_work_decode(p, mla_work_raw(p, pos)).n_units;
   }
-  const int n_units = (t1 - t0 + kMlaUnit - 1) / kMlaUnit;
-  const int n_tiles = (n_units + 1) / 2;
-  const int n_pages = (L + p.bs - 1) / p.bs;
-  constexpr uint32_t kPHalfBytes = kMlaOwn * 64 + kMlaOwn * 4;  // P rows + factors of 64 heads
+  // the cluster's r-th work; false past the end
+  auto mla_work = [&](const MlaParams&, int, int, int, int r, MlaWork& w) -> bool {
+    const long long pos = mla_work_pos(cl, G, r);
+    if (pos >= n_work) return false;
+    w = mla_work_decode(p, r < kMlaWorkCache ? sWorks[r] : mla_work_raw(p, pos));
+    return true;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < MlaBar::kCount; ++i) mbar_init(&bars[i], MlaBar::arrivals(i));
     *abort_flag = 0;
+    // the first unit of each set: expect the peer's 32 KB of partial scores
+    for (int k = 0; k < 2; ++k)
+      if (k < g_total) mbar_arrive_expect_tx(&rx_full[k], Sh::kSlotB);
     fence_barrier_init();
-    // arm the receive slots for the first units and the final statistics
-    for (int x = 0; x < kMlaNX; ++x) mbar_arrive_expect_tx(&rx_full[x], Sh::kXBuf);
-    for (int x = 0; x < kMlaNP; ++x) mbar_arrive_expect_tx(&p_remote[x], kPHalfBytes);
-    mbar_arrive_expect_tx(stat_full, kMlaOwn * 8);
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, kMlaTmemCols);
     tmem_relinquish();
   }
@@ -323,511 +340,527 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   };
   auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-  if (warp == 8) {
+  // Q_r of head row hr (lane of quarter q) in work w: latent dims 256 r .. 256 r + 255
+  // into TMEM columns kTmQ.. as bf16 pairs (the raw row words), rope dims
+  // 512 + 32 r .. + 31 into row hr of the 64-byte-swizzled shared tile (chunk c at
+  // c ^ ((row >> 1) & 3)).  Run by a warpgroup (all four lane quarters); arrives on q_full.
+  auto q_row = [&](const MlaWork& w, int hr, bool& valid) -> const uint4* {
+    const int head = w.ht * kMlaRows + hr;
+    valid = hr < p.hrows && head < p.H;
+    return p.q + ((size_t)w.s * p.H + (valid ? head : 0)) * (kMlaDq / 8);
+  };
+  auto load_q = [&](const MlaWork& w, int quarter) {
+    const int hr = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    bool row_valid;
+    const uint4* src = q_row(w, hr, row_valid);
+    for (int c0 = 0; c0 < 128; c0 += 64) {  // two rounds of 16 loads (the row is 36 chunks; rope last)
+      uint32_t v[64];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 x4 = row_valid ? __ldg(src + 32 * rank + c0 / 4 + i) : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * i] = x4.x, v[4 * i + 1] = x4.y, v[4 * i + 2] = x4.z, v[4 * i + 3] = x4.w;
+      }
+      tmem_st32(lane_base + kTmQ + c0, v);
+      tmem_st32(lane_base + kTmQ + c0 + 32, v + 32);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x4 = row_valid ? __ldg(src + kMlaDv / 8 + 4 * rank + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sQr + hr * 64 + ((c ^ ((hr >> 1) & 3)) << 4)) = x4;
+    }
+    fence_proxy_async_smem();  // the score UMMA reads the rope tile through the async proxy
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(q_full);
+  };
+  // warm L2 with a work's query row (its 576 B in this CTA's half: 256 latent + 32 rope dims)
+  auto prefetch_q = [&](const MlaWork& w, int hr) {
+    bool row_valid;
+    const uint4* src = q_row(w, hr, row_valid);
+    if (!row_valid) return;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) prefetch_l2(src + 32 * rank + 8 * c);
+    prefetch_l2(src + kMlaDv / 8 + 4 * rank);
+  };
+  // the next non-empty work at or after list position r (false: none)
+  auto next_nonempty = [&](int r, MlaWork& w) -> bool {
+    for (; mla_work(p, n_work, cl, G, r, w); ++r)
+      if (w.n_units > 0) return true;
+    return false;
+  };
+
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     regs_dec<kMlaRegsLow>();
-    // Per unit and page piece: lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3,
-    // lane 5 pi + 4 the rope half block 512 + 32 r .. + 31.
-    const int32_t* bt_row = p.block_table + (size_t)s * p.max_blocks;
+    // Per unit and page piece (R rows: the block size, at most 64, or at most 32
+    // when partitions start on odd multiples of 32 tokens, so a piece never crosses
+    // a page): lanes 5 pi + 0..3 load the latent blocks 4 r .. 4 r + 3, lane 5 pi + 4
+    // the rope half block 512 + 32 r .. + 31.
     if (lane == 0) {
       tma_prefetch_desc(&tmKV);
       tma_prefetch_desc(&tmKVh);
     }
-    const int R = min(p.bs, kMlaUnit);  // rows per box
+    const int R = p.box_rows;
     const int pieces = kMlaUnit / R;
     const int pi = lane / 5, lb = lane - pi * 5;
     const uint64_t pol = l2_policy_evict_first();
-    int issued = 0;
-    for (int u = 0; u < n_units; ++u) {
-      const int st = u % kMlaStages;
-      const int tok = t0 + u * kMlaUnit + pi * R;
-      const int pg = tok / p.bs;
-      const bool live = pi < pieces && pg < n_pages;
-      int rowc = 0;
-      if (live) {
-        const int b = checked_block(bt_row, pg, p.num_blocks, &g_status_mla);
-        rowc = b < 0 ? -R : b * p.bs + (tok - pg * p.bs);
+    int g = 0;
+    bool ok = true;
+    MlaWork w;
+    for (int r = 0; ok && mla_work(p, n_work, cl, G, r, w); ++r) {
+      const int32_t* bt_row = p.block_table + (size_t)w.s * p.max_blocks;
+      for (int u = 0; u < w.n_units; ++u, ++g) {
+        const int st = g % kMlaStages;
+        const int tok = w.t0 + u * kMlaUnit + pi * R;
+        const bool live = pi < pieces && tok < w.t1;
+        int rowc = 0;
+        if (live) {
+          const int pg = tok / p.bs;
+          const int b = checked_block(bt_row, pg, p.num_blocks, &g_status_mla);
+          rowc = b < 0 ? -R : b * p.bs + (tok - pg * p.bs);
+        }
+        const uint32_t n_live = (uint32_t)__popc(__ballot_sync(0xffffffffu, live && lb == 0));
+        if (g >= kMlaStages && !wait_all(&kv_empty[st], ((g / kMlaStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], n_live * (uint32_t)(R * (4 * 128 + 64)));
+        __syncwarp();
+        if (live) {
+          if (lb < 4)
+            tma_load_3d(sKV + st * Sh::kStage + lb * Sh::kBlk + pi * R * 128, &tmKV, &kv_full[st],
+                        (4 * (int)rank + lb) * 64, 0, rowc, pol);
+          else
+            tma_load_3d(sRope + st * Sh::kRopeU + pi * R * 64, &tmKVh, &kv_full[st], kMlaDv + 32 * (int)rank, 0,
+                        rowc, pol);
+        }
       }
-      const uint32_t n_live = (uint32_t)__popc(__ballot_sync(0xffffffffu, live && lb == 0));
-      if (u >= kMlaStages && !wait_all(&kv_empty[st], ((u / kMlaStages) - 1) & 1)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], n_live * (uint32_t)(R * (4 * 128 + 64)));
-      __syncwarp();
-      if (live) {
-        if (lb < 4)
-          tma_load_3d(sKV + (lb * kMlaStages + st) * Sh::kBlk + pi * R * 128, &tmKV, &kv_full[st],
-                      (4 * (int)rank + lb) * 64, 0, rowc, pol);
-        else
-          tma_load_3d(sRope + st * Sh::kRopeU + pi * R * 64, &tmKVh, &kv_full[st], kMlaDv + 32 * (int)rank, 0, rowc,
-                      pol);
-      }
-      ++issued;
     }
+    // after an abort, let the copies already on their way land before the CTA exits
     if (*abort_flag)
-      for (int u = max(0, issued - kMlaStages); u < issued; ++u)
-        mbar_wait(&kv_full[u % kMlaStages], (u / kMlaStages) & 1, &g_status_mla);
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ UMMA issuer
+      for (int v = max(0, g - kMlaStages); v < g; ++v)
+        mbar_wait(&kv_full[v % kMlaStages], (v / kMlaStages) & 1, &g_status_mla);
+  } else if (warp == 13 || warp == 14) {
+    // ------------------------------------------------------------ UMMA issuers
+    // Warp 13 issues the score UMMAs, warp 14 the P V UMMAs, each blocking on its own
+    // next barrier (the two streams touch disjoint TMEM: S buffers, O).
     regs_dec<kMlaRegsLow>();
-    constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kMlaRows, kMlaTile, false, false);
+    constexpr uint32_t kIdQK = umma_idesc_bf16_f32(kMlaRows, kMlaUnit, false, false);
     constexpr uint32_t kIdPV = umma_idesc_bf16_f32(kMlaRows, kMlaHalf, false, true);
-    const uint32_t kv = smem_u32(sKV), rope = smem_u32(sRope), qr = smem_u32(sQr), pt = smem_u32(sP);
-    bool issued = false;
-    auto qk = [&](int j) {  // partial S_j = Q_r K_r^T over this CTA's 288 key dimensions, 64 tokens
-      if (lane == 0) {
-        const int s0 = (2 * j) % kMlaStages;
-        const uint32_t d_tmem = tmem + kTmS + (j & 1) * kMlaTile;
+    const uint32_t kv = smem_u32(sKV), rope = smem_u32(sRope), qr = smem_u32(sQr), slot = smem_u32(sSlot);
+    const uint16_t peer_mask = (uint16_t)(1u << peer);
+    const bool scores = warp == 13;
+    bool issued = false, ok = true;
+    int g = 0, qi = 0;  // global unit, non-empty works before the current one
+    MlaWork w;
+    for (int r = 0; ok && mla_work(p, n_work, cl, G, r, w); ++r) {
+      if (w.n_units == 0) continue;
+      for (int u = 0; u < w.n_units; ++u, ++g) {
+        const int k = g & 1;
+        const int st = g % kMlaStages;
+        if (scores) {
+          // partial S of unit g into S[k] over this CTA's 288 key dimensions, once the
+          // work's Q is in place, the set owning S[k] has read its previous unit and
+          // the latent has landed
+          if ((g >= 2 && !wait_all(&s_free[k], ((g - 2) >> 1) & 1)) || (u == 0 && !wait_all(q_full, qi & 1)) ||
+              !wait_all(&kv_full[st], (g / kMlaStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if (lane == 0) {
+            const uint32_t d_tmem = tmem + kTmS + k * kMlaUnit;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          umma_bf16_tmem_a(d_tmem, tmem + kTmQ + kk * 8,
-                           umma_desc_sw128(kv + ((kk >> 2) * kMlaStages + s0) * Sh::kBlk + (kk & 3) * 32, 16, 1024),
-                           kIdQK, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 16; ++kk)
+              umma_bf16_tmem_a(d_tmem, tmem + kTmQ + kk * 8,
+                               umma_desc_sw128(kv + st * Sh::kStage + (kk >> 2) * Sh::kBlk + (kk & 3) * 32, 16, 1024),
+                               kIdQK, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          umma_bf16(d_tmem, umma_desc_sw64(qr + kk * 32, 512), umma_desc_sw64(rope + s0 * Sh::kRopeU + kk * 32, 512),
-                    kIdQK, 1u);
-        umma_commit(&s_full[j & 1]);
-      }
-    };
-    auto wait_tile = [&](int j) -> bool {  // the latent units of tile j have landed
-      const int u0 = 2 * j;
-      if (!wait_all(&kv_full[u0 % kMlaStages], (u0 / kMlaStages) & 1)) return false;
-      if (u0 + 1 < n_units && !wait_all(&kv_full[(u0 + 1) % kMlaStages], ((u0 + 1) / kMlaStages) & 1)) return false;
-      tc_fence_after_sync();
-      return true;
-    };
-    bool ok = wait_all(q_full, 0);
-    if (ok) tc_fence_after_sync();
-    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-      if (!wait_tile(j)) {
-        ok = false;
-        break;
-      }
-      qk(j);
-      issued = true;
-      __syncwarp();
-    }
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (j + 2 < n_tiles) {  // QK_{j+2} into S[j & 1] once the row warps have read tile j
-        if (!wait_all(&s_free[j & 1], (j >> 1) & 1) || !wait_tile(j + 2)) {
-          ok = false;
-          break;
-        }
-        qk(j + 2);
-        __syncwarp();
-      }
-      for (int h = 0; ok && h < 2; ++h) {
-        const int u = 2 * j + h;
-        if (u >= n_units) break;
-        const int x = u % kMlaNP;
-        if (!wait_all(&p_relay[x], (u / kMlaNP) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const int st = u % kMlaStages;
-        const int tok0 = t0 + u * kMlaUnit;
-        if (tok0 + kMlaUnit > t1) {
-          // rows past the partition end (NaN tails, pieces not loaded): zero the value columns
-          for (int row = (t1 - tok0) + lane; row < kMlaUnit; row += 32)
-            for (int b = 0; b < 4; ++b) {
-              uint4* d = reinterpret_cast<uint4*>(sKV + (b * kMlaStages + st) * Sh::kBlk + row * 128);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) d[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          fence_proxy_async_smem();
+            for (int kk = 0; kk < 2; ++kk)
+              umma_bf16(d_tmem, umma_desc_sw64(qr + kk * 32, 512),
+                        umma_desc_sw64(rope + st * Sh::kRopeU + kk * 32, 512), kIdQK, 1u);
+            umma_commit(&s_full[k]);
+          }
           __syncwarp();
-        }
-        if (lane == 0) {
+          issued = true;
+        } else {
+          // O_r (+)= P V of unit g, once its references are replayed (and, for a work's
+          // first unit, once the previous work's O has been read out)
+          if (!wait_all(&p_go[k], (g >> 1) & 1) || (u == 0 && qi > 0 && !wait_all(o_free, (qi - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const int tok0 = w.t0 + u * kMlaUnit;
+          if (tok0 + kMlaUnit > w.t1) {
+            // value rows past the work's end (cache tails, pieces not loaded): zero them,
+            // since 0 * NaN would reach O (their scores are masked already)
+            for (int row = (w.t1 - tok0) + lane; row < kMlaUnit; row += 32)
+              for (int b = 0; b < 4; ++b) {
+                uint4* d = reinterpret_cast<uint4*>(sKV + st * Sh::kStage + b * Sh::kBlk + row * 128);
 #pragma unroll
-          for (int kk = 0; kk < kMlaUnit / 16; ++kk)
-            umma_bf16(tmem + kTmO, umma_desc_sw64(pt + x * Sh::kPBuf + kk * 32, 512),
-                      umma_desc_sw128(kv + st * Sh::kBlk + kk * 2048, kMlaStages * Sh::kBlk, 1024), kIdPV,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&pv_done[u % 4]);
-          umma_commit(&kv_empty[st]);
+                for (int q = 0; q < 8; ++q) d[q] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            const uint32_t pt = slot + k * Sh::kSlotB;
+#pragma unroll
+            for (int kk = 0; kk < kMlaUnit / 16; ++kk)
+              umma_bf16(tmem + kTmO, umma_desc_sw128(pt + kk * 32, 16, Sh::kPGroup),
+                        umma_desc_sw128(kv + st * Sh::kStage + kk * 16 * 128, Sh::kBlk, 1024), kIdPV,
+                        (u > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&kv_empty[st]);
+            umma_commit(&pv_done[k]);
+            // the slot of this unit is free again: the peer may send its partial of unit g + 2
+            if (g + 2 < g_total) umma_commit_multicast(&tx_ok[k], peer_mask);
+          }
+          __syncwarp();
+          issued = true;
         }
-        __syncwarp();
       }
+      ++qi;
     }
     if (!ok && issued) {
-      if (lane == 0) umma_commit(drain);
+      uint64_t* d = drain + (scores ? 0 : 1);
+      if (lane == 0) umma_commit(d);
       __syncwarp();
-      mbar_wait(drain, 0, &g_status_mla);
+      mbar_wait(d, 0, &g_status_mla);
     }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ score exchange
-    regs_dec<kMlaRegsLow>();
-    const uint32_t peer_rx = dsmem_map(smem_u32(sRx), peer);
-    const uint32_t peer_rx_full = dsmem_map(smem_u32(rx_full), peer);
-    const uint32_t peer_tx_ok = dsmem_map(smem_u32(tx_ok), peer);
-    int armed[kMlaNX];
-#pragma unroll
-    for (int x = 0; x < kMlaNX; ++x) armed[x] = x < n_units ? x : -1;
-    for (int t = 0; t <= n_units; ++t) {
-      if (t < n_units) {  // staged unit t -> the peer's receive slot t % kMlaNX
-        const int x = t % kMlaNX;
-        if (!wait_all(&staged[x], (t / kMlaNX) & 1)) break;
-        if (lane == 0)
-          bulk_copy_to_peer(peer_rx + x * Sh::kXBuf, smem_u32(sStg) + x * Sh::kXBuf, Sh::kXBuf, peer_rx_full + x * 8);
-        __syncwarp();
-      }
-      const int u = t - 1;  // credit: this CTA has read unit u, so the peer may send unit u + kMlaNX
-      if (u >= 0 && u + kMlaNX < n_units) {
-        const int x = u % kMlaNX;
-        if (!wait_all(&rx_read[x], (u / kMlaNX) & 1)) break;
-        // Relaxed: the credit orders nothing but the row warps' reads of the receive
-        // slot, which returned before their rx_read arrival (release).
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&rx_full[x], Sh::kXBuf);
-          mbar_arrive_remote_relaxed(peer_tx_ok + x * 8);
-        }
-#pragma unroll
-        for (int y = 0; y < kMlaNX; ++y)
-          if (y == x) armed[y] = u + kMlaNX;
-        __syncwarp();
-      }
-    }
-    // after an abort, let the peer's copies already on their way land before this CTA exits
-    if (lane == 0 && *abort_flag) {
-#pragma unroll
-      for (int x = 0; x < kMlaNX; ++x)
-        if (armed[x] >= 0) mbar_wait(&rx_full[x], (armed[x] / kMlaNX) & 1, &g_status_mla);
-    }
-  } else if (warp == 11) {
-    // ------------------------------------------------------------ P exchange
-    regs_dec<kMlaRegsLow>();
-    const uint32_t peer_p = dsmem_map(smem_u32(sP), peer);
-    const uint32_t peer_alpha = dsmem_map(smem_u32(sAlpha), peer);
-    const uint32_t peer_p_remote = dsmem_map(smem_u32(p_remote), peer);
-    const uint32_t peer_pslot_ok = dsmem_map(smem_u32(pslot_ok), peer);
-    const uint32_t own_a = (uint32_t)(rank * kMlaOwn * 4);
-    int armed[kMlaNP];
-#pragma unroll
-    for (int x = 0; x < kMlaNP; ++x) armed[x] = x < n_units ? x : -1;
-    bool ok = true;
-    for (int t = 0; ok && t <= n_units; ++t) {
-      if (t < n_units) {  // P rows + factors of own heads for unit t -> the peer's P slot t % kMlaNP
-        const int x = t % kMlaNP;
-        if (!wait_all(&p_local[x], (t / kMlaNP) & 1) ||
-            (t >= kMlaNP && !wait_all(&pslot_ok[x], ((t / kMlaNP) - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        if (lane < 4) {  // own heads occupy lanes 32 q + 16 r .. + 15 of each quarter q: 16 rows x 64 B
-          const uint32_t off = x * Sh::kPBuf + (uint32_t)(32 * lane + 16 * rank) * 64;
-          bulk_copy_to_peer(peer_p + off, smem_u32(sP) + off, 16 * 64, peer_p_remote + x * 8);
-        } else if (lane == 4) {
-          bulk_copy_to_peer(peer_alpha + x * kMlaRows * 4 + own_a, smem_u32(sAlpha) + x * kMlaRows * 4 + own_a,
-                            kMlaOwn * 4, peer_p_remote + x * 8);
-        }
-        __syncwarp();
-      }
-      const int u = t - 1;  // credit: P V of unit u completed, so the peer may send unit u + kMlaNP
-      if (u >= 0 && u + kMlaNP < n_units) {
-        const int x = u % kMlaNP;
-        if (!wait_all(&pv_done[u % 4], (u / 4) & 1)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&p_remote[x], kPHalfBytes);
-          mbar_arrive_remote_relaxed(peer_pslot_ok + x * 8);
-        }
-#pragma unroll
-        for (int y = 0; y < kMlaNP; ++y)
-          if (y == x) armed[y] = u + kMlaNP;
-        __syncwarp();
-      }
-    }
-    // final row statistics of own heads -> the peer
-    if (ok && wait_all(stat_local, 0) && lane == 0)
-      bulk_copy_to_peer(dsmem_map(smem_u32(sStat), peer) + rank * kMlaOwn * 8, smem_u32(sStat) + rank * kMlaOwn * 8,
-                        kMlaOwn * 8, dsmem_map(smem_u32(stat_full), peer));
-    __syncwarp();
-    if (lane == 0 && *abort_flag) {
-#pragma unroll
-      for (int x = 0; x < kMlaNP; ++x)
-        if (armed[x] >= 0) mbar_wait(&p_remote[x], (armed[x] / kMlaNP) & 1, &g_status_mla);
-      mbar_wait(stat_full, 0, &g_status_mla);
-    }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ rescale warps
     regs_dec<kMlaRegsLow>();
-    const int quarter = warp - 4;
-    const int hh = 64 * (lane >> 4) + 16 * quarter + (lane & 15);  // head (in the tile) of this lane
+    const int quarter = warp - 8;
+    const int hr = quarter * 32 + lane;  // head row of this lane = its TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    // Q_r of this lane's head in work w: latent dims 256 r .. 256 r + 255 into TMEM
+    // columns kTmQ.. as bf16 pairs (the raw row words), rope dims 512 + 32 r .. + 31
+    // into row hr of the 64-byte-swizzled shared tile (chunk c at c ^ ((row >> 1) & 3)).
     bool ok = true;
-    for (int t = 0; ok && t < n_units; ++t) {
-      const int x = t % kMlaNP;
-      if (!wait_all(&p_local[x], (t / kMlaNP) & 1) || !wait_all(&p_remote[x], (t / kMlaNP) & 1)) {
+    int g = 0;
+    int qi = 0;  // non-empty works completed
+    {
+      MlaWork w0;
+      if (next_nonempty(0, w0)) load_q(w0, quarter);  // later works: loaded by a row-warp set
+    }
+    MlaWork w;
+    for (int r = 0; ok && mla_work(p, n_work, cl, G, r, w); ++r) {
+      const int head = w.ht * kMlaRows + hr;
+      const bool row_valid = hr < p.hrows && head < p.H;
+      const size_t sh = (size_t)w.s * p.H + head;
+      if (w.L_raw > p.cap && rank == 0 && w.ht == 0 && w.part == 0 && hr == 0)
+        atomicOr(&g_status_mla, METIS_STATUS_SEQ_TOO_LONG);
+      if (w.n_units == 0) {
+        // nothing readable: an empty sequence gets 0 / -inf, an empty partition lse = -inf
+        if (row_valid) {
+          if (w.direct) {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf;
+            for (int c = 0; c < kMlaHalf; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0u, 0u, 0u, 0u);
+            if (rank == 0 && p.lse_out) p.lse_out[sh] = -INFINITY;
+          } else if (rank == 0) {
+            p.part_lse[sh * p.max_parts + w.part] = -INFINITY;
+          }
+        }
+        continue;
+      }
+      MlaWork w2;
+      if (next_nonempty(r + 1, w2)) prefetch_q(w2, hr);
+      float C = -INFINITY, Lsum = 0.f;
+      for (int u = 0; ok && u < w.n_units; ++u, ++g) {
+        const int k = g & 1;
+        if (!wait_all(&p_full[k], (g >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const float c = sTagC[k * kMlaRows + hr];
+        const float l = sTagL[k * kMlaRows + hr];
+        float fo = 1.f;
+        if (u == 0) {
+          C = c;
+          Lsum = l;
+        } else if (c > C) {
+          fo = exp2_approx(C - c);
+          Lsum = fmaf(Lsum, fo, l);
+          C = c;
+        } else if (c < C) {
+          // this unit exponentiated against a smaller reference: bring its P down to C
+          const float gsc = exp2_approx(c - C);
+          uint8_t* prow = sSlot + k * Sh::kSlotB + (hr >> 3) * Sh::kPGroup + (hr & 7) * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4* q4 = reinterpret_cast<uint4*>(prow + (j << 4));
+            uint4 v = *q4;
+            uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&wv[i]));
+              wv[i] = pack_bf16x2(f.x * gsc, f.y * gsc);
+            }
+            *q4 = v;
+          }
+          fence_proxy_async_smem();  // P V reads P through the async proxy
+          Lsum = fmaf(l, gsc, Lsum);
+        } else {
+          Lsum += l;
+        }
+        if (__any_sync(0xffffffffu, fo != 1.f)) {
+          // O holds every earlier unit of the work once P V of unit g - 1 completed
+          if (!wait_all(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c32 = 0; c32 < kMlaHalf / 32; ++c32) {
+            uint32_t ov[32];
+            tmem_ld32(lane_base + kTmO + c32 * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * fo);
+            tmem_st32(lane_base + kTmO + c32 * 32, ov);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&p_go[k]);
+      }
+      if (!ok) break;
+      // epilogue: O_r / l and the lse, once the work's last P V completed
+      if (!wait_all(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
         ok = false;
         break;
       }
-      const float a = sAlpha[x * kMlaRows + hh];
-      if (t >= 1 && __any_sync(0xffffffffu, a != 1.0f)) {
-        // O holds every earlier unit only once P V of unit t - 1 completed
-        if (!wait_all(&pv_done[(t - 1) % 4], ((t - 1) / 4) & 1)) {
+      tc_fence_after_sync();
+      const float inv = 1.0f / Lsum;
+      // Each thread holds its own row; a 4 x 4 transpose of 32-byte chunks inside each
+      // group of four lanes lets a warp store write 8 rows x 128 contiguous bytes
+      // (instead of 32 rows x 32 bytes).  Lane 4 q + i then holds chunk i of rows
+      // 4 q .. 4 q + 3 of its warp's 32.
+      const int gq = lane >> 2, gi = lane & 3;
+      auto transpose4 = [&](uint32_t* wv) {
+        const int b0 = lane & 1, b1 = (lane >> 1) & 1;
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t x = b0 ? wv[8 * (2 * sl) + k] : wv[8 * (2 * sl + 1) + k];
+            const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 1);
+            if (b0)
+              wv[8 * (2 * sl) + k] = y;
+            else
+              wv[8 * (2 * sl + 1) + k] = y;
+          }
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t x = b1 ? wv[8 * sl + k] : wv[8 * (2 + sl) + k];
+            const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 2);
+            if (b1)
+              wv[8 * sl + k] = y;
+            else
+              wv[8 * (2 + sl) + k] = y;
+          }
+      };
+      if (w.direct) {
+        // 64 bf16 columns (128 B) per row and step
+#pragma unroll 1
+        for (int c64 = 0; c64 < kMlaHalf / 64; ++c64) {
+          uint32_t ov[64], wv[32];
+          tmem_ld32(lane_base + kTmO + c64 * 64, ov);
+          tmem_ld32(lane_base + kTmO + c64 * 64 + 32, ov + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            wv[j] = pack_bf16x2(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
+          transpose4(wv);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int rr = quarter * 32 + 4 * gq + c;  // the row this lane writes a chunk of
+            const int hd = w.ht * kMlaRows + rr;
+            if (rr < p.hrows && hd < p.H)
+              st_global_v8(reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)w.s * p.H + hd) * kMlaDv +
+                               rank * kMlaHalf + c64 * 64 + gi * 16,
+                           wv + 8 * c);
+          }
+        }
+      } else {
+        // 32 fp32 columns (128 B) per row and step
+#pragma unroll 1
+        for (int c32 = 0; c32 < kMlaHalf / 32; ++c32) {
+          uint32_t wv[32];
+          tmem_ld32(lane_base + kTmO + c32 * 32, wv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) wv[j] = __float_as_uint(__uint_as_float(wv[j]) * inv);
+          transpose4(wv);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int rr = quarter * 32 + 4 * gq + c;
+            const int hd = w.ht * kMlaRows + rr;
+            if (rr < p.hrows && hd < p.H)
+              st_global_v8(p.part_out + (((size_t)w.s * p.H + hd) * p.max_parts + w.part) * kMlaDv + rank * kMlaHalf +
+                               c32 * 32 + gi * 8,
+                           wv + 8 * c);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(o_free);  // the next work's first P V may overwrite O
+      ++qi;
+      if (row_valid && rank == 0) {
+        const float lse = (C + log2f(Lsum)) * kLn2;
+        if (w.direct) {
+          if (p.lse_out) p.lse_out[sh] = lse;
+        } else {
+          p.part_lse[sh * p.max_parts + w.part] = lse;
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ row warps
+    regs_inc<kMlaRegsRow>();
+    const int set = warp >> 2;
+    const int quarter = warp & 3;
+    const int hr = quarter * 32 + lane;  // head row of this lane = its TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* my_slot = sSlot + set * Sh::kSlotB;
+    // scores of this lane: chunk j at j * 512 + lane * 16 within the warp's part
+    const uint32_t peer_part = dsmem_map(smem_u32(my_slot), peer) + quarter * Sh::kWarpB + lane * 16;
+    const uint8_t* rx_part = my_slot + quarter * Sh::kWarpB + lane * 16;
+    const uint32_t peer_rx_full = dsmem_map(smem_u32(&rx_full[set]), peer);
+    uint8_t* prow = my_slot + (hr >> 3) * Sh::kPGroup + (hr & 7) * 128;   // inside this warp's part
+    const int sw8 = hr & 7;
+    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    bool ok = true;
+    int g0 = 0;  // first unit of the current work
+    MlaWork w;
+    for (int r = 0; ok && mla_work(p, n_work, cl, G, r, w); g0 += w.n_units, ++r) {
+      float c_prev = -INFINITY;  // c_{u-2}: this set's reference of its previous unit of the work
+      const int u_first = (set - g0) & 1;  // this set takes the units with g = g0 + u of its parity
+      for (int u = u_first; u < w.n_units; u += 2) {
+        const int g = g0 + u;
+        const uint32_t ph = (g >> 1) & 1;
+        // R_{u-2} = max(R_{u-3}, c_{u-2}) within the work; R_{u-3} comes from the other
+        // set, which published a value as it started unit g - 1 (every unit publishes,
+        // so the hand-over is the same at work boundaries).  Publish R_{u-2}.
+        float r3 = -INFINITY;
+        if (g >= 1) {
+          if (!wait_all(&ref_full[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          r3 = sRef[((g - 1) & 1) * kMlaRows + hr];
+        }
+        const float base = u >= 2 ? fmaxf(u >= 3 ? r3 : -INFINITY, c_prev) : -INFINITY;
+        sRef[set * kMlaRows + hr] = base;
+        mbar_arrive(&ref_full[set]);
+        // this CTA's partial scores of the unit
+        if (!wait_all(&s_full[set], ph)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < kMlaHalf / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + kTmO + c * 32, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
-          tmem_st32(lane_base + kTmO + c * 32, ov);
+        uint32_t sv[kMlaUnit];
+        tmem_ld32(lane_base + kTmS + set * kMlaUnit, sv);
+        tmem_ld32(lane_base + kTmS + set * kMlaUnit + 32, sv + 32);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&s_free[set]);
+        // ... into the peer's slot (free again once the peer's P V of unit g - 2 completed)
+        if (g >= 2 && !wait_all(&tx_ok[set], ((g >> 1) - 1) & 1)) {
+          ok = false;
+          break;
         }
-        tmem_st_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          st_async_v4(peer_part + j * 512, sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3], peer_rx_full);
+        // the peer's partial of the same unit, in this CTA's slot
+        if (!wait_all(&rx_full[set], ph)) {
+          ok = false;
+          break;
+        }
+        // expect the peer's partial of this set's next unit (it can only come after
+        // this unit's P V, which follows everything below)
+        if (quarter == 0 && lane == 0 && g + 2 < g_total) mbar_arrive_expect_tx(&rx_full[set], Sh::kSlotB);
+        // full scores, scaled into the log2 domain: x = (own + peer) * scale * log2(e)
+        float x[kMlaUnit];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float4 r4 = *reinterpret_cast<const float4*>(rx_part + j * 512);
+          const uint64_t a = f2_mul(f2_add(f2_pack(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])),
+                                           f2_pack(r4.x, r4.y)), sl2x2);
+          const uint64_t b = f2_mul(f2_add(f2_pack(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])),
+                                           f2_pack(r4.z, r4.w)), sl2x2);
+          f2_unpack(a, x[4 * j], x[4 * j + 1]);
+          f2_unpack(b, x[4 * j + 2], x[4 * j + 3]);
+        }
+        __syncwarp();  // the warp's scores are read before its P overwrites them
+        const int vis = min(kMlaUnit, w.t1 - (w.t0 + u * kMlaUnit));
+        if (vis < kMlaUnit) {
+#pragma unroll
+          for (int i = 0; i < kMlaUnit; ++i) x[i] = i < vis ? x[i] : -INFINITY;
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < kMlaUnit; i += 8) {
+          m4[0] = max3f(m4[0], x[i], x[i + 1]);
+          m4[1] = max3f(m4[1], x[i + 2], x[i + 3]);
+          m4[2] = max3f(m4[2], x[i + 4], x[i + 5]);
+          m4[3] = max3f(m4[3], x[i + 6], x[i + 7]);
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float c = mx <= base + kMlaSlack ? base : mx;  // the unit's maximum also when base = -inf
+        c_prev = c;
+        const uint64_t negc = f2_pack(-c, -c);
+        uint64_t l2[2] = {0ull, 0ull};
+        uint32_t pk[kMlaUnit / 2];
+#pragma unroll
+        for (int i = 0; i < kMlaUnit; i += 2) {
+          float d0, d1;
+          f2_unpack(f2_add(f2_pack(x[i], x[i + 1]), negc), d0, d1);
+          const float e0 = exp2_approx(d0);
+          const float e1 = exp2_approx(d1);
+          l2[(i >> 1) & 1] = f2_add(l2[(i >> 1) & 1], f2_pack(e0, e1));
+          pk[i >> 1] = pack_bf16x2(e0, e1);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(prow + ((j ^ sw8) << 4)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                                                                          pk[4 * j + 3]);
+        float la, lb, lc, ld;
+        f2_unpack(l2[0], la, lb);
+        f2_unpack(l2[1], lc, ld);
+        sTagC[set * kMlaRows + hr] = c;
+        sTagL[set * kMlaRows + hr] = (la + lb) + (lc + ld);
+        fence_proxy_async_smem();  // P V reads P through the async proxy
+        mbar_arrive(&p_full[set]);
       }
-      tc_fence_before_sync();
-      mbar_arrive(&p_relay[x]);
+      if (!ok) break;
+      // The set that does not take the work's last unit would next wait for scores that
+      // need the next work's Q: it loads that Q, as soon as the work's last score UMMA
+      // (the last reader of the current Q) has completed.
+      const int g_last = g0 + w.n_units - 1;
+      MlaWork w2;
+      if (w.n_units > 0 && ((g_last & 1) ^ 1) == set && next_nonempty(r + 1, w2)) {
+        if (!wait_all(&s_full[g_last & 1], (g_last >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        load_q(w2, quarter);
+      }
     }
   } else {
-    // ------------------------------------------------------------ row warps
-    // Two sets over the same lanes: warps 0-3 take the even units, warps 12-15 the
-    // odd ones; the running max passes from set to set after every unit.
-    regs_inc<kMlaRegsRow>();
-    const int set = warp >> 3;
-    const int quarter = warp & 3;
-    const int g = lane >> 4, li = lane & 15;
-    const bool own = g == (int)rank;
-    const int xi = 16 * quarter + li;               // row within a 64-head half
-    const int hh = 64 * g + xi;                      // head (in the tile) of this lane
-    const int head = h0 + hh;
-    const bool row_valid = hh < p.hrows && head < p.H;
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int prow = 32 * quarter + 16 * (int)rank + li;  // P row / TMEM lane of the own head this lane works on
-    const int tok_half = own ? 0 : 16;                // tokens of a unit this lane exponentiates
-    if (set == 0) {
-      // Q_r of this lane's head: latent dims 256 r .. 256 r + 255 into TMEM columns
-      // kTmQ.. as bf16 pairs (the raw row words), rope dims 512 + 32 r .. + 31 into
-      // row `lane` of the 64-byte-swizzled shared tile (chunk c at c ^ ((row >> 1) & 3)).
-      const uint4* src = p.q + ((size_t)s * p.H + (row_valid ? head : 0)) * (kMlaDq / 8);
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 x4 = row_valid ? __ldg(src + 32 * rank + c0 / 4 + i) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * i] = x4.x, v[4 * i + 1] = x4.y, v[4 * i + 2] = x4.z, v[4 * i + 3] = x4.w;
-        }
-        tmem_st32(lane_base + kTmQ + c0, v);
-      }
-      const int row = 32 * quarter + lane;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 x4 = row_valid ? __ldg(src + kMlaDv / 8 + 4 * rank + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sQr + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = x4;
-      }
-      fence_proxy_async_smem();  // the score UMMA reads the rope tile through the async proxy
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(q_full);
-    }
-    const float sl2 = p.scale_log2;
-    const float sgn = sl2 < 0.f ? -1.f : 1.f;
-    const float asl2 = fmaxf(fabsf(sl2), 1e-30f);
-    auto load_s = [&](int u, uint32_t* v) -> bool {  // this CTA's partial scores of unit u, every lane
-      const int j = u >> 1;
-      if (!wait_all(&s_full[j & 1], (j >> 1) & 1)) return false;
-      tc_fence_after_sync();
-      tmem_ld32(lane_base + kTmS + (j & 1) * kMlaTile + (u & 1) * kMlaUnit, v);
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&s_free[j & 1]);  // each unit of a tile is read once, by the set that owns it
-      return true;
-    };
-    auto stage = [&](int u, const uint32_t* v) -> bool {  // the peer's heads of unit u -> staging slot
-      const int x = u % kMlaNX;
-      if (u >= kMlaNX && !wait_all(&tx_ok[x], ((u / kMlaNX) - 1) & 1)) return false;
-      if (!own) {
-        uint8_t* dst = sStg + x * Sh::kXBuf + xi * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(dst + ((c ^ (xi & 7)) << 4)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        fence_proxy_async_smem();  // the bulk copy reads through the async proxy
-      }
-      mbar_arrive(&staged[x]);
-      return true;
-    };
-    // The running max after unit v (processed by the other set): take it, and bring
-    // this set's share of the row sum, kept relative to the max it last saw, up to date.
-    auto catch_up = [&](int v, float& m_run, float& l_run) -> bool {
-      const int other = set ^ 1;
-      if (!wait_all(&hand[other * 4 + quarter], (v >> 1) & 1)) return false;
-      const float m_o = sHand[other * kMlaRows + quarter * 32 + lane];
-      if (m_o > m_run) {
-        l_run *= exp2_approx(m_run - m_o);  // 0 when nothing was seen yet (m_run = -inf, l_run = 0)
-        m_run = m_o;
-      }
-      return true;
-    };
-    uint32_t cur[kMlaUnit], nxt[kMlaUnit];
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = set < n_units ? load_s(set, cur) && stage(set, cur) : true;
-    for (int u = set; ok && u < n_units; u += 2) {
-      const int x = u % kMlaNX;
-      if (!wait_all(&rx_full[x], (u / kMlaNX) & 1)) {
-        ok = false;
-        break;
-      }
-      float sc[kMlaUnit];
-      if (own) {
-        const uint8_t* rx = sRx + x * Sh::kXBuf + xi * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 r4 = *reinterpret_cast<const float4*>(rx + ((c ^ (xi & 7)) << 4));
-          sc[4 * c] = __uint_as_float(cur[4 * c]) + r4.x;
-          sc[4 * c + 1] = __uint_as_float(cur[4 * c + 1]) + r4.y;
-          sc[4 * c + 2] = __uint_as_float(cur[4 * c + 2]) + r4.z;
-          sc[4 * c + 3] = __uint_as_float(cur[4 * c + 3]) + r4.w;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kMlaUnit; ++c) sc[c] = 0.f;
-      }
-      mbar_arrive(&rx_read[x]);
-      // lane pair (i, i ^ 16) splits the own head's unit: the own lane keeps tokens 0..15,
-      // the partner takes tokens 16..31
-      float mine[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float hi = __shfl_xor_sync(0xffffffffu, sc[16 + k], 16);
-        mine[k] = own ? sc[k] : hi;
-      }
-      const int vis = min(kMlaUnit, t1 - (t0 + u * kMlaUnit)) - tok_half;  // visible tokens among mine
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < 16; ++c) mx[c & 3] = fmaxf(mx[c & 3], c < vis ? mine[c] * sgn : -INFINITY);
-      float mxa = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 16));
-      // the max after unit u - 1 comes from the other set
-      if (u >= 1 && !catch_up(u - 1, m_run, l_run)) {
-        ok = false;
-        break;
-      }
-      const float m_new = fmaxf(m_run, mxa == -INFINITY ? -INFINITY : mxa * asl2);
-      float alpha = 1.f;
-      if (m_new > m_run + 8.0f) {
-        alpha = exp2_approx(m_run - m_new);
-        m_run = m_new;
-      }
-      l_run *= alpha;
-      sHand[set * kMlaRows + quarter * 32 + lane] = m_run;
-      mbar_arrive(&hand[set * 4 + quarter]);  // release: the other set may take unit u + 1
-      // this set's next unit: scores from TMEM, the peer's heads staged (after this
-      // unit's receive, so the two CTAs' credits never wait on each other)
-      if (u + 2 < n_units && !(load_s(u + 2, nxt) && stage(u + 2, nxt))) {
-        ok = false;
-        break;
-      }
-      const float neg_m = -m_run;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[8];
-#pragma unroll
-      for (int c = 0; c < 16; c += 2) {
-        const float e0 = c < vis ? exp2_approx(fmaf(mine[c] * sgn, asl2, neg_m)) : 0.f;
-        const float e1 = c + 1 < vis ? exp2_approx(fmaf(mine[c + 1] * sgn, asl2, neg_m)) : 0.f;
-        ls[c & 3] += e0;
-        ls[(c + 1) & 3] += e1;
-        pk[c >> 1] = pack_bf16x2(e0, e1);
-      }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // P slot u % kMlaNP is free once P V of unit u - kMlaNP completed
-      const int xp = u % kMlaNP;
-      if (u >= kMlaNP && !wait_all(&pv_done[(u - kMlaNP) % 4], ((u - kMlaNP) / 4) & 1)) {
-        ok = false;
-        break;
-      }
-      uint8_t* pr = sP + xp * Sh::kPBuf + prow * 64;
-      const int sw = (prow >> 1) & 3, c0 = own ? 0 : 2;
-      *reinterpret_cast<uint4*>(pr + ((c0 ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(pr + (((c0 + 1) ^ sw) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      if (own) sAlpha[xp * kMlaRows + hh] = alpha;
-      fence_proxy_async_smem();  // P V and the bulk copy read P through the async proxy
-      mbar_arrive(&p_local[xp]);
-#pragma unroll
-      for (int c = 0; c < kMlaUnit; ++c) cur[c] = nxt[c];
-    }
-    // the max after the last unit, for the set that did not process it
-    if (ok && ((n_units - 1) & 1) != set) ok = catch_up(n_units - 1, m_run, l_run);
-    float* sL = sHand + 2 * kMlaRows;
-    if (set == 1) {
-      // hand this set's share of the row sums to set 0, which writes the rows
-      sL[quarter * 32 + lane] = l_run;
-      mbar_arrive(fin);
-      ok = false;
-    } else if (ok && wait_all(fin, 0)) {
-      l_run += sL[quarter * 32 + lane];
-    } else {
-      ok = false;
-    }
-    if (ok && wait_all(&pv_done[(n_units - 1) % 4], ((n_units - 1) / 4) & 1)) {
-      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // the own head's row sum
-      if (own) {
-        sStat[hh * 2] = m_run;
-        sStat[hh * 2 + 1] = l_tot;
-        fence_proxy_async_smem();  // copied to the peer by the bulk engine
-      }
-      mbar_arrive(stat_local);
-      // this lane's row: an own head (local statistics) or a peer head (the peer's)
-      bool have = true;
-      float inv = 0.f;
-      if (own) {
-        inv = 1.0f / l_tot;
-      } else {
-        have = false;
-      }
-      if (!__all_sync(0xffffffffu, have)) {
-        if (!wait_all(stat_full, 0)) ok = false;
-        if (!own) inv = 1.0f / sStat[hh * 2 + 1];
-      }
-      if (ok) {
-        tc_fence_after_sync();
-        const size_t sh = (size_t)s * p.H + head;
-#pragma unroll 1
-        for (int c = 0; c < kMlaHalf / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + kTmO + c * 32, ov);
-          tmem_ld_wait();
-          if (!row_valid) continue;
-          if (direct) {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + sh * kMlaDv + rank * kMlaHalf + c * 32;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
-              *reinterpret_cast<uint4*>(o + i) = v;
-            }
-          } else {
-            float* o = p.part_out + (sh * p.max_parts + part) * kMlaDv + rank * kMlaHalf + c * 32;
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(o + i) =
-                  make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                              __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-          }
-        }
-        if (row_valid && own) {
-          const float lse = (m_run + log2f(l_tot)) * kLn2;
-          if (direct) {
-            if (p.lse_out) p.lse_out[sh] = lse;
-          } else {
-            p.part_lse[sh * p.max_parts + part] = lse;
-          }
-        }
-      }
-    }
+    regs_dec<kMlaRegsLow>();  // warp 15: no role
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kMlaTmemCols);
   }
@@ -898,11 +931,11 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   if (num_seqs > 65535) return fail(METIS_E_SHAPE, "num_seqs must be <= 65535");
   if ((long long)max_blocks * block_size > 0x7fffffffLL || (long long)num_blocks * block_size > 0x7fffffffLL)
     return fail(METIS_E_SHAPE, "max_blocks * block_size and num_blocks * block_size must fit in int32");
-  if (partition_size < 0 || partition_size % kMlaUnit)
+  if (partition_size < 0 || partition_size % kMlaAlign)
     return fail(METIS_E_SHAPE, "partition_size must be 0 or a positive multiple of 32");
-  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 32) || !aligned(block_table, 4) ||
       !aligned(seq_lens, 4) || !aligned(lse_out, 4))
-    return fail(METIS_E_ALIGN, "tensors must be 16-byte aligned (index arrays and lse_out: 4-byte)");
+    return fail(METIS_E_ALIGN, "q and kv_cache must be 16-byte aligned, out 32-byte, index arrays and lse_out 4-byte");
   if (!(scale == scale)) return fail(METIS_E_SHAPE, "scale is NaN");
   const MlaWorkspace lay = mla_workspace_layout(num_seqs, num_heads, max_seq_len, partition_size);
   if (!workspace || workspace_bytes < lay.total || !aligned(workspace, 256))
@@ -936,14 +969,16 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   p.scale_log2 = scale * kLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+  // 64-row boxes (fewer, larger TMA copies) when every unit starts on a multiple of 64 tokens
+  p.box_rows = std::min(block_size, (partition_size % kMlaUnit == 0) ? kMlaUnit : kMlaAlign);
   CUtensorMap tmKV, tmKVh;
   const uint64_t kdims[3] = {(uint64_t)kMlaDq, 1, (uint64_t)num_blocks * block_size};
   const uint64_t kstr[2] = {(uint64_t)kMlaDq * 2, (uint64_t)kMlaDq * 2};
-  const uint32_t kbox[3] = {64, 1, (uint32_t)std::min(block_size, kMlaUnit)};
+  const uint32_t kbox[3] = {64, 1, (uint32_t)p.box_rows};
   int rc = encode_tiled(&tmKV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, kbox,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  const uint32_t khbox[3] = {32, 1, (uint32_t)std::min(block_size, kMlaUnit)};
+  const uint32_t khbox[3] = {32, 1, (uint32_t)p.box_rows};
   rc = encode_tiled(&tmKVh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, kdims, kstr, khbox,
                     CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
@@ -966,8 +1001,14 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
                   (2 * kMlaRegsRow + 2 * kMlaRegsLow) / 4);
     regs_checked = 1;
   }
-  rc = launch_dependent(mla_decode_kernel, dim3((unsigned)(lay.max_items * head_tiles * 2)), dim3(kMlaThreads),
-                        MlaShape::kSmem, st, "mla_decode_kernel launch", tmKV, tmKVh, p);
+  // persistent: one cluster (two SMs) per SM pair, each walking its share of the work list
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return fail(METIS_E_CUDA, "SM count: %s", cudaGetErrorString(ce));
+  const size_t clusters = std::max<size_t>(1, std::min<size_t>((size_t)(sms / 2), lay.max_items * head_tiles));
+  rc = launch_dependent(mla_decode_kernel, dim3((unsigned)(clusters * 2)), dim3(kMlaThreads), MlaShape::kSmem, st,
+                        "mla_decode_kernel launch", tmKV, tmKVh, p);
   if (rc) return rc;
   if (partition_size > 0 && lay.max_parts > 1)
     rc = launch_merge_ex(p.part_out, p.part_lse, seq_lens, partition_size, out, lse_out, num_seqs, num_heads, kMlaDv,

@@ -104,6 +104,16 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Arrive on the mbarrier at the same shared-memory offset in every CTA of
+// `cta_mask` (this cluster) once every UMMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMEM <-> registers: 32 lanes x 32 consecutive 32-bit columns per warp
 // (thread i of the warp gets lane base+i).  A warp may only touch the lane

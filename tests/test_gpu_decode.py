@@ -213,6 +213,36 @@ def test_seq_longer_than_max_seq_len_is_flagged():
 # the merge entry point on its own
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("D,P", [(64, 40), (128, 300), (512, 40), (128, 2500)])
+def test_merge_many_partitions_against_oracle(D, P):
+    """The many-partition merge (one CTA per row, weights cached for the first 2048 partitions, recomputed
+    past them): empty partitions inside the range (NaN rows never read), partitions past the length,
+    empty sequences."""
+    rng = np.random.default_rng(D + P)
+    S, H, psize = 4, 3, 16
+    part_out = rng.standard_normal((S, H, P, D)).astype(np.float32)
+    part_lse = (rng.standard_normal((S, H, P)) * 3).astype(np.float32)
+    lens = np.array([P * psize, psize * (P - 3) + 5, 0, 17 * psize + 1], dtype=np.int32)
+    for k in (1, P // 2, P - 5):                              # empty partitions inside the range
+        part_lse[0, :, k] = -np.inf
+        part_out[0, :, k] = np.nan
+    part_out[1, :, P - 2:] = np.nan                           # partitions past the length
+    part_out[3, :, 18:] = np.nan
+    out, lse = pa.metis_merge_attn_states(torch.from_numpy(part_out).cuda(), torch.from_numpy(part_lse).cuda(),
+                                          torch.from_numpy(lens).cuda(), psize, want_lse=True)
+    torch.cuda.synchronize()
+    for s in range(S):
+        n = min(P, -(-int(lens[s]) // psize)) if lens[s] > 0 else 0
+        if n == 0:
+            ref_o = np.zeros((H, D))
+            ref_l = np.full(H, -np.inf)
+        else:
+            ref_o, ref_l = oracle.merge_states(part_out[s, :, :n].transpose(1, 0, 2).astype(np.float64),
+                                               part_lse[s, :, :n].T.astype(np.float64))
+        assert_parity(out[s], ref_o, torch.float32)
+        assert_lse(lse[s], ref_l, torch.float32)
+
+
 @pytest.mark.parametrize("D", [64, 128, 512])
 def test_merge_attn_states_against_oracle(D):
     rng = np.random.default_rng(D)

@@ -12,7 +12,7 @@ from helpers import assert_lse, assert_parity, dev, f64, replace_blocks
 pytestmark = pytest.mark.gpu
 
 # the partition size bench.py uses for the MLA workload
-BENCH_MLA_PARTITION = 3072
+BENCH_MLA_PARTITION = 2048
 
 
 @pytest.fixture(autouse=True)
