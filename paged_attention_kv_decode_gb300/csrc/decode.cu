@@ -48,13 +48,26 @@ struct DecodeParams {
   int partition_size;
   int max_parts;
   int cap;  // tokens readable per sequence: min(max_blocks * bs, max_seq_len)
+  // Decodes of a chunked-prefill batch (NULL otherwise): the batch's cu_q_lens.
+  // Sequence s is handled only if rows[s + 1] - rows[s] == 1; its query, output
+  // and lse row is rows[s] of the packed [T, H, D] tensors.
+  const int32_t* rows;
 };
+
+// Output (and query) row of sequence s; -1 when the call skips it (a sequence
+// with more than one query token in a mixed batch).
+__device__ __forceinline__ int decode_row(const DecodeParams& p, int s) {
+  if (!p.rows) return s;
+  const int r0 = p.rows[s];
+  return p.rows[s + 1] - r0 == 1 ? r0 : -1;
+}
 
 // Token range of this CTA, after clamping the sequence length.  Returns
 // false when the CTA has nothing to do (after writing what an empty
 // partition or sequence must leave behind).
 template <typename OutT>
-__device__ __forceinline__ bool decode_range(const DecodeParams& p, int part, int g, int s, int& t0, int& t1) {
+__device__ __forceinline__ bool decode_range(const DecodeParams& p, int part, int g, int s, int orow, int& t0,
+                                             int& t1) {
   int L_raw = p.seq_lens[s];
   int L = L_raw;
   if (L > p.cap) {
@@ -75,9 +88,9 @@ __device__ __forceinline__ bool decode_range(const DecodeParams& p, int part, in
     if (L_raw > 0 && t0 < L_raw && threadIdx.x < p.r)
       p.part_lse[((size_t)s * p.H + g * p.r + threadIdx.x) * p.max_parts + part] = -INFINITY;
   } else {
-    OutT* o = reinterpret_cast<OutT*>(p.out) + ((size_t)s * p.H + (size_t)g * p.r) * p.D;
+    OutT* o = reinterpret_cast<OutT*>(p.out) + ((size_t)orow * p.H + (size_t)g * p.r) * p.D;
     for (int i = threadIdx.x; i < p.r * p.D; i += blockDim.x) o[i] = OutT(0.0f);
-    if (p.lse_out && threadIdx.x < p.r) p.lse_out[(size_t)s * p.H + g * p.r + threadIdx.x] = -INFINITY;
+    if (p.lse_out && threadIdx.x < p.r) p.lse_out[(size_t)orow * p.H + g * p.r + threadIdx.x] = -INFINITY;
   }
   return false;
 }
@@ -104,7 +117,7 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 // split-KV partial.
 template <typename OutT, int NW>
 __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const float* cm, const float* cl,
-                                                  const float* co, int part, int g, int s) {
+                                                  const float* co, int part, int g, int s, int orow) {
   const int D = p.D;
   const int nq = D / 4;
   for (int idx = threadIdx.x; idx < p.r * nq; idx += NW * 32) {
@@ -134,9 +147,9 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const f
       *reinterpret_cast<float4*>(dst) = make_float4(a0 * inv, a1 * inv, a2 * inv, a3 * inv);
       if (d == 0) p.part_lse[((size_t)s * p.H + head) * p.max_parts + part] = lse;
     } else {
-      OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)s * p.H + head) * D + d;
+      OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)orow * p.H + head) * D + d;
       store4<OutT>(dst, a0 * inv, a1 * inv, a2 * inv, a3 * inv);
-      if (d == 0 && p.lse_out) p.lse_out[(size_t)s * p.H + head] = lse;
+      if (d == 0 && p.lse_out) p.lse_out[(size_t)orow * p.H + head] = lse;
     }
   }
 }
@@ -168,7 +181,9 @@ constexpr int bf16_decode_smem_bytes() {
 constexpr int kMaxRankSeqs = 128;
 
 __device__ __forceinline__ int seq_of_rank(const DecodeParams& p, int rank, int* lens, int* found) {
-  for (int i = threadIdx.x; i < p.S; i += blockDim.x) lens[i] = min(max(p.seq_lens[i], 0), p.cap);
+  // sequences the call skips rank last
+  for (int i = threadIdx.x; i < p.S; i += blockDim.x)
+    lens[i] = decode_row(p, i) < 0 ? -1 : min(max(p.seq_lens[i], 0), p.cap);
   if (threadIdx.x == 0) *found = rank;
   __syncthreads();
   for (int c = threadIdx.x; c < p.S; c += blockDim.x) {
@@ -202,8 +217,10 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   const int s = (p.partition_size == 0 && p.S <= kMaxRankSeqs) ? seq_of_rank(p, blockIdx.z, rank_lens, &rank_found)
                                                                 : (int)blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int orow = decode_row(p, s);
+  if (orow < 0) return;  // not a decode of this mixed batch
   int t0, t1;
-  if (!decode_range<__nv_bfloat16>(p, part, g, s, t0, t1)) return;
+  if (!decode_range<__nv_bfloat16>(p, part, g, s, orow, t0, t1)) return;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
@@ -256,7 +273,7 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   {
     const bool live = rA < p.r;
     const __nv_bfloat16* qrow =
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)s * p.H + g * p.r + (live ? rA : 0)) * D;
+        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)orow * p.H + g * p.r + (live ? rA : 0)) * D;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       qf[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * q4) : 0u;
@@ -386,7 +403,7 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
     c1[1] = o[mt][3];
   }
   __syncthreads();
-  combine_and_store<__nv_bfloat16, NW>(p, cm, cl, co, part, g, s);
+  combine_and_store<__nv_bfloat16, NW>(p, cm, cl, co, part, g, s, orow);
 }
 
 // ---------------------------------------------------------------------------
@@ -406,7 +423,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
   const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int t0, t1;
-  if (!decode_range<float>(p, part, g, s, t0, t1)) return;
+  if (!decode_range<float>(p, part, g, s, s, t0, t1)) return;
 
   const float* q = reinterpret_cast<const float*>(p.q) + ((size_t)s * p.H + (size_t)g * p.r) * D;
   float qv[8][DPL];
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
 #pragma unroll
     for (int i = 0; i < DPL; ++i) co[((size_t)warp * D + lane * DPL + i) * 8 + h] = o[h][i];
   __syncthreads();
-  combine_and_store<float, kF32Warps>(p, cm, cl, co, part, g, s);
+  combine_and_store<float, kF32Warps>(p, cm, cl, co, part, g, s, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -767,6 +784,37 @@ static int launch_bf16(const DecodeParams& p, const void* k_cache, const void* v
   return check_launch("decode_bf16_kernel launch");
 }
 
+// The single-token sequences of a chunked-prefill batch, through the decode
+// kernel (unsplit, longest first): rows = the batch's cu_q_lens.  The caller has
+// validated the shapes (bf16, head_dim 64 or 128, head ratio 1, 2, 4 or 8).
+int launch_decode_rows(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H, int G,
+                       int D, int bs, int max_blocks, int num_blocks, float scale, int cap, cudaStream_t st) {
+  DecodeParams p;
+  p.q = q;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse_out = lse_out;
+  p.part_out = nullptr;
+  p.part_lse = nullptr;
+  p.S = S;
+  p.H = H;
+  p.G = G;
+  p.D = D;
+  p.bs = bs;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.r = H / G;
+  p.scale_log2 = scale * kLog2e;
+  p.partition_size = 0;
+  p.max_parts = 1;
+  p.cap = cap;
+  p.rows = rows;
+  const dim3 grid(1u, (unsigned)G, (unsigned)S);
+  return D == 64 ? launch_bf16<64>(p, k_cache, v_cache, grid, st) : launch_bf16<128>(p, k_cache, v_cache, grid, st);
+}
+
 }  // namespace metis
 
 using namespace metis;
@@ -838,6 +886,7 @@ static int paged_decode(const void* q, const void* k_cache, const void* v_cache,
   p.partition_size = partition_size;
   p.max_parts = parts ? (int)parts : 1;
   p.cap = eff_len;
+  p.rows = nullptr;
   if (parts) {
     const size_t units = (size_t)num_seqs * num_heads * parts;
     p.part_out = reinterpret_cast<float*>(workspace);

@@ -59,6 +59,12 @@ int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t*
                     float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int skip_single,
                     cudaStream_t st);
 
+// The single-token sequences of a chunked-prefill batch through the bf16 decode
+// kernel (decode.cu); rows = the batch's cu_q_lens.  Other sequences are skipped.
+int launch_decode_rows(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H, int G,
+                       int D, int bs, int max_blocks, int num_blocks, float scale, int cap, cudaStream_t st);
+
 // Per-translation-unit device status words.
 int decode_status(uint32_t* bits, int clear);
 int prefill_status(uint32_t* bits, int clear);

@@ -8,7 +8,9 @@
 // q_len = cu_q_lens[s+1] - cu_q_lens[s] of which are queried; query i sits at
 // position L - q_len + i and sees every key t <= L - q_len + i (the cached
 // prefix plus a causal mask inside the chunk).  Single-token decodes are the
-// q_len = 1 case and run through the same tiles.
+// q_len = 1 case: with a head ratio up to 8 the entry point hands them to the
+// decode kernel (memory-bound, 16-token page units per warp) and lists no tiles
+// for them here; above 8 they run through the same tiles.
 //
 // Tiling.  A query tile is 128 rows of one KV head's group: the r = H/G query
 // heads times 128/r consecutive query tokens (GQA packing).  One CTA per SM
@@ -39,7 +41,7 @@
 // already implies "PV_w_{j-1} finished", so the rescale never waits.
 //
 // Persistent mixed batch: a small schedule kernel lists the (sequence,
-// query-tile pair) items heaviest first -- chunks and single-token decodes in one
+// query-tile pair) items heaviest first -- the chunks of every length in one
 // list -- and one CTA per SM takes units (item, KV head) from that list as it
 // goes (warp 14 claims the next one with an atomic and publishes it to the other
 // warps through a two-slot ring).  Every role keeps its ring and barrier counters
@@ -95,6 +97,7 @@ struct PrefillParams {
   int* unit_head;   // next unit to hand out (the schedule kernel zeroes it)
   int S, T, H, G, r, Tq, bs, max_blocks, num_blocks, cap;
   float scale_log2;
+  int skip_decodes;  // single-token sequences are served by the decode kernel: list no tiles for them
 };
 
 // Shared-memory layout (all tiles 128-byte swizzled, [64-column half][row][128 B]).
@@ -171,8 +174,9 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   int local = 0;
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
-    pf_lengths(p, s, L, q_len, false);
-    local += (q_len + pair_tokens - 1) / pair_tokens;
+    const bool routed = p.skip_decodes && p.cu_q_lens[s + 1] - p.cu_q_lens[s] == 1;
+    pf_lengths(p, s, L, q_len, routed);  // a routed decode's content errors are flagged here
+    if (!routed) local += (q_len + pair_tokens - 1) / pair_tokens;
   }
   scan[tid] = local;
   __syncthreads();
@@ -188,7 +192,8 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
     pf_lengths(p, s, L, q_len, false);
-    const int np = (q_len + pair_tokens - 1) / pair_tokens;
+    const bool routed = p.skip_decodes && p.cu_q_lens[s + 1] - p.cu_q_lens[s] == 1;
+    const int np = routed ? 0 : (q_len + pair_tokens - 1) / pair_tokens;
     for (int t = 0; t < np; ++t, ++pos) {
       if (pos >= total) break;
       const int work = pf_kv_tiles(L, q_len, 2 * t, p.Tq) + pf_kv_tiles(L, q_len, 2 * t + 1, p.Tq);
@@ -826,6 +831,17 @@ extern "C" int metis_paged_attn_prefill_chunk(const void* q, const int32_t* cu_q
   p.cap = (int)std::min<long long>((long long)max_blocks * block_size, (long long)max_seq_len);
   p.scale_log2 = scale * kLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // Single-token sequences (the decodes of a mixed batch) go through the decode
+  // kernel, which streams their K/V at the memory rate (a 128-row query tile would
+  // hold r valid rows of them).  It runs first, as an ordinary launch; the schedule
+  // and the chunk kernel follow it.  Head ratios above 8 stay on the chunk path.
+  p.skip_decodes = r <= 8 && num_seqs <= 65535;
+  if (p.skip_decodes) {
+    const int rc = launch_decode_rows(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse_out, num_seqs,
+                                      num_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale,
+                                      p.cap, st);
+    if (rc) return rc;
+  }
   return head_dim == 128 ? launch_prefill<128>(p, q, k_cache, v_cache, workspace, max_items, st)
                          : launch_prefill<64>(p, q, k_cache, v_cache, workspace, max_items, st);
 }
