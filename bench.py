@@ -792,6 +792,72 @@ def other_workloads(names, reps, dev, flush, stream, peak_hbm, peaks_tc, oracle_
                            "note": "the chunked-prefill step's new K/V rows scattered into their pages"}
         del key, value, kc, vc, slots, c
         torch.cuda.empty_cache()
+    if "kvw_step" in names:
+        # the paged K/V write chained in front of attention (the write kernel lets the
+        # attention call launch early; it waits for the write before reading the cache):
+        # (a) the batched-decode step: each sequence's newest token written, then decode;
+        # (b) the chunked-prefill step: its 8,240 new rows written, then the mixed call
+        res["kv_write_then_attention"] = {}
+        c = wl.config2_batched_decode()
+        t = [x.to(dev) for x in (c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
+        out = torch.empty_like(t[0])
+        lens = c.seq_lens.numpy().astype(np.int64)
+        bt = c.block_table.numpy()
+        last = lens - 1
+        slots = torch.from_numpy(bt[np.arange(c.S), last // c.bs].astype(np.int64) * c.bs + last % c.bs).to(dev)
+        g = torch.Generator().manual_seed(13)
+        key = torch.randn(c.S, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
+        value = torch.randn(c.S, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
+
+        def dec():
+            pa.metis_paged_attn_decode(*t, c.scale, out=out, max_seq_len=c.max_seq_len, stream=stream)
+
+        def wdec():
+            pa.metis_reshape_and_cache(key, value, t[1], t[2], slots, stream=stream)
+            dec()
+
+        d_ms, _ = _time_calls(dec, reps, flush, stream, "decode_alone")
+        wd_ms, _ = _time_calls(wdec, reps, flush, stream, "write_then_decode")
+        res["kv_write_then_attention"]["batched_decode"] = {
+            "decode_ms": d_ms, "write_then_decode_ms": wd_ms, "added_us": (wd_ms - d_ms) * 1e3, "new_rows": c.S,
+            "note": "each sequence's newest K/V row written into its page, then the unsplit decode"}
+        del t, out, key, value, slots, c
+        c = wl.config4_chunked_prefill()
+        t = [x.to(dev) for x in (c.q, c.cu_q_lens, c.k_cache, c.v_cache, c.block_table, c.seq_lens)]
+        out = torch.empty_like(t[0])
+        ws = torch.empty(pa.metis_prefill_workspace_bytes(c.S, c.T, c.H, c.G), dtype=torch.uint8, device=dev)
+        cu = c.cu_q_lens.numpy()
+        lens = c.seq_lens.numpy().astype(np.int64)
+        bt = c.block_table.numpy()
+        sl = []
+        for si in range(c.S):
+            ql = int(cu[si + 1] - cu[si])
+            tt = np.arange(lens[si] - ql, lens[si])
+            sl.append(bt[si, tt // c.bs].astype(np.int64) * c.bs + tt % c.bs)
+        slots = torch.from_numpy(np.concatenate(sl)).to(dev)
+        key = torch.randn(c.T, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
+        value = torch.randn(c.T, c.G, c.D, generator=g).to(torch.bfloat16).to(dev)
+
+        def pf():
+            pa.metis_paged_attn_prefill_chunk(*t, c.scale, out=out, max_seq_len=c.max_seq_len, workspace=ws,
+                                              stream=stream)
+
+        def wpf():
+            pa.metis_reshape_and_cache(key, value, t[2], t[3], slots, stream=stream)
+            pf()
+
+        def w_only():
+            pa.metis_reshape_and_cache(key, value, t[2], t[3], slots, stream=stream)
+
+        p_ms, _ = _time_calls(pf, reps, flush, stream, "prefill_alone")
+        w_ms, _ = _time_calls(w_only, reps, flush, stream, "write_alone")
+        wp_ms, _ = _time_calls(wpf, reps, flush, stream, "write_then_prefill")
+        res["kv_write_then_attention"]["chunked_prefill"] = {
+            "prefill_ms": p_ms, "write_ms": w_ms, "write_then_prefill_ms": wp_ms,
+            "added_us": (wp_ms - p_ms) * 1e3, "hidden_us": (p_ms + w_ms - wp_ms) * 1e3, "new_rows": c.T,
+            "note": "the step's new K/V rows written into their pages, then the mixed chunked-prefill call"}
+        del t, out, ws, key, value, slots, c
+        torch.cuda.empty_cache()
     if "pfx" in names:
         # prefix-cache page keys + lookup-or-allocate over a batch of prompts sharing system prompts
         c = wl.prefix_workload()
@@ -903,8 +969,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=PARTITION)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workloads", default="c1,c3,c4,c5,kvw,pfx",
-                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw,pfx; "
+    ap.add_argument("--workloads", default="c1,c3,c4,c5,kvw,kvw_step,pfx",
+                    help="other workloads to time after the main one (comma list of c1,c3,c4,c5,kvw,kvw_step,pfx; "
                          "empty: none)")
     ap.add_argument("--workload-reps", type=int, default=20)
     ap.add_argument("--skip-main", action="store_true",

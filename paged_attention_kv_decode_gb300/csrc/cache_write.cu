@@ -28,6 +28,9 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(const uint4* __r
                                                                 uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                                 const int64_t* __restrict__ slot_mapping,
                                                                 int row_vecs, long long total_slots) {
+  // The attention call that follows may start launching now: it waits for this
+  // grid (pdl_wait) before it reads the cache.
+  pdl_launch_dependents();
   const int n = blockIdx.x;
   const long long slot = slot_mapping[n];
   if (slot < 0) return;  // padding token
@@ -54,6 +57,7 @@ __global__ void __launch_bounds__(128) mla_reshape_and_cache_kernel(const uint4*
                                                                     const int64_t* __restrict__ slot_mapping,
                                                                     int lat_vecs, int rope_vecs,
                                                                     long long total_slots) {
+  pdl_launch_dependents();  // as in reshape_and_cache_kernel
   const int n = blockIdx.x;
   const long long slot = slot_mapping[n];
   if (slot < 0) return;

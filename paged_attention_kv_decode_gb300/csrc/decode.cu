@@ -206,6 +206,9 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   constexpr int KS = Shape::kSteps;
   static_assert(NW * (64 + D * 32) <= NW * STAGES * STAGE_BYTES, "combine area must fit in the ring");
   pdl_launch_dependents();  // the merge may start launching; it waits for this grid to finish
+  // Launched as a programmatic dependent (e.g. of the paged K/V write): every input
+  // is read after the previous grid in the stream has completed.
+  pdl_wait();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
@@ -417,6 +420,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
                                                                      const DecodeParams p) {
   constexpr int DPL = D / 32;  // dims per lane
   pdl_launch_dependents();
+  pdl_wait();  // inputs are read after the previous grid in the stream has completed
   __shared__ float cm[kF32Warps * 8], cl[kF32Warps * 8];
   __shared__ float co[kF32Warps * D * 8];
 
@@ -780,8 +784,8 @@ static int launch_bf16(const DecodeParams& p, const void* k_cache, const void* v
   auto kern = decode_bf16_kernel<D, kBf16Warps, kBf16Stages>;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem, &done);
   if (rc) return rc;
-  kern<<<grid, kBf16Warps * 32, smem, st>>>(tmK, tmV, p);
-  return check_launch("decode_bf16_kernel launch");
+  return launch_dependent(kern, grid, dim3(kBf16Warps * 32), (size_t)smem, st, "decode_bf16_kernel launch", tmK, tmV,
+                          p);
 }
 
 // The single-token sequences of a chunked-prefill batch, through the decode
@@ -903,11 +907,10 @@ static int paged_decode(const void* q, const void* k_cache, const void* v_cache,
   if (dtype == METIS_F32) {
     const float* kc = reinterpret_cast<const float*>(k_cache);
     const float* vc = reinterpret_cast<const float*>(v_cache);
-    if (head_dim == 64)
-      decode_f32_kernel<64><<<grid, kF32Warps * 32, 0, st>>>(kc, vc, p);
-    else
-      decode_f32_kernel<128><<<grid, kF32Warps * 32, 0, st>>>(kc, vc, p);
-    rc = check_launch("decode_f32_kernel launch");
+    rc = head_dim == 64 ? launch_dependent(decode_f32_kernel<64>, grid, dim3(kF32Warps * 32), 0, st,
+                                           "decode_f32_kernel launch", kc, vc, p)
+                        : launch_dependent(decode_f32_kernel<128>, grid, dim3(kF32Warps * 32), 0, st,
+                                           "decode_f32_kernel launch", kc, vc, p);
   } else {
     rc = head_dim == 64 ? launch_bf16<64>(p, k_cache, v_cache, grid, st) : launch_bf16<128>(p, k_cache, v_cache, grid, st);
   }

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, i
   __shared__ int scan[1024];
   __shared__ int4 buf[kMlaSortMax];
   pdl_launch_dependents();  // the attention kernel may start launching (it waits for the items)
+  pdl_wait();  // a programmatic dependent itself: inputs are read once the previous grid completed
   const int tid = threadIdx.x;
   const int per = (p.S + 1023) / 1024;
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
@@ -983,8 +984,9 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
                     CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
 
-  mla_schedule_kernel<<<1, 1024, 0, st>>>(p, items, count, (int)lay.max_items);
-  rc = check_launch("mla_schedule_kernel launch");
+  // a programmatic dependent of the kernel before it (e.g. the latent-cache write)
+  rc = launch_dependent(mla_schedule_kernel, dim3(1), dim3(1024), 0, st, "mla_schedule_kernel launch", p, items, count,
+                        (int)lay.max_items);
   if (rc) return rc;
   static int done = 0;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), MlaShape::kSmem, &done);

@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   __shared__ int scan[kSchedThreads];
   __shared__ int4 buf[kSortMax];
   pdl_launch_dependents();  // the attention kernel may start launching (it waits for the items)
+  pdl_wait();  // a programmatic dependent itself: inputs are read once the previous grid completed
   const int tid = threadIdx.x;
   const int per = (p.S + kSchedThreads - 1) / kSchedThreads;
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
@@ -737,8 +738,10 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
   if (rc) return rc;
   rc = encode_tiled(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v_cache, kdims, kstr, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  prefill_schedule_kernel<<<1, kSchedThreads, 0, st>>>(p, items, count, (int)max_items);
-  rc = check_launch("prefill_schedule_kernel launch");
+  // a programmatic dependent of the kernel before it (the paged K/V write, or the
+  // decodes of this batch): its launch overlaps that kernel's tail
+  rc = launch_dependent(prefill_schedule_kernel, dim3(1), dim3(kSchedThreads), 0, st, "prefill_schedule_kernel launch",
+                        p, items, count, (int)max_items);
   if (rc) return rc;
   constexpr int smem = PfShape<D>::kSmem;
   static int done = 0;
