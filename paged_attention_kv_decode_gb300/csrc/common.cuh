@@ -262,6 +262,34 @@ __device__ __forceinline__ float warp_sum_xor(float v, int from_mask) {
   return v;
 }
 
+// Exclusive prefix sum of one value per thread over a block of NT threads (NT a
+// multiple of 32, at most 1024); *total receives the sum.  warp_sums: NT / 32
+// ints of shared memory.  Two block barriers.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NT / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NT / 32) warp_sums[lane] = w;  // inclusive sums of the warp totals
+  }
+  __syncthreads();
+  *total = warp_sums[NT / 32 - 1];
+  return x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+}
+
 // Physical block of a sequence's logical page, validated against the pool.
 // Returns -1 (and flags the status word) for an id outside [0, num_blocks).
 __device__ __forceinline__ int checked_block(const int32_t* row, int page, int num_blocks, unsigned int* status) {

@@ -667,22 +667,32 @@ __global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* 
 #pragma unroll
   for (int j = 0; j < kMergeMaxD / 128; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!empty) {
+    // kMergeUnroll partitions per step, so that many row loads per lane are in
+    // flight at once (one at a time, the sum waits on memory latency)
     const float4* prow = reinterpret_cast<const float4*>(part_out + sh * max_parts * D);
-    for (int i = 0; i < n; ++i) {
-      const float x = lrow[i];
-      if (!(x > -INFINITY)) continue;
-      const float w = exp2_approx(fmaf(x, kLog2e, -M2));
+    for (int i0 = 0; i0 < n; i0 += kMergeUnroll) {
+      float w[kMergeUnroll];
+      float4 v[kMergeUnroll][kMergeMaxD / 128];
 #pragma unroll
-      for (int j = 0; j < kMergeMaxD / 128; ++j) {
-        const int c = lane + 32 * j;
-        if (c < nq) {
-          const float4 v = __ldg(prow + (size_t)i * nq + c);
-          acc[j].x = fmaf(w, v.x, acc[j].x);
-          acc[j].y = fmaf(w, v.y, acc[j].y);
-          acc[j].z = fmaf(w, v.z, acc[j].z);
-          acc[j].w = fmaf(w, v.w, acc[j].w);
+      for (int k = 0; k < kMergeUnroll; ++k) {
+        const int i = i0 + k;
+        const float x = i < n ? lrow[i] : -INFINITY;
+        w[k] = x > -INFINITY ? exp2_approx(fmaf(x, kLog2e, -M2)) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kMergeMaxD / 128; ++j) {
+          const int c = lane + 32 * j;
+          v[k][j] = (w[k] != 0.f && c < nq) ? __ldg(prow + (size_t)i * nq + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+#pragma unroll
+      for (int k = 0; k < kMergeUnroll; ++k)
+#pragma unroll
+        for (int j = 0; j < kMergeMaxD / 128; ++j) {
+          acc[j].x = fmaf(w[k], v[k][j].x, acc[j].x);
+          acc[j].y = fmaf(w[k], v[k][j].y, acc[j].y);
+          acc[j].z = fmaf(w[k], v[k][j].z, acc[j].z);
+          acc[j].w = fmaf(w[k], v[k][j].w, acc[j].w);
+        }
     }
   }
   const float inv = empty ? 0.f : 1.0f / W;

@@ -153,7 +153,7 @@ __device__ __forceinline__ int mla_parts(const MlaParams& p, int L_raw) {
 
 __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, int4* items, int* count,
                                                             int max_items) {
-  __shared__ int scan[1024];
+  __shared__ int warp_sums[32];
   __shared__ int4 buf[kMlaSortMax];
   pdl_launch_dependents();  // the attention kernel may start launching (it waits for the items)
   pdl_wait();  // a programmatic dependent itself: inputs are read once the previous grid completed
@@ -162,17 +162,10 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, i
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
   int local = 0;
   for (int s = s0; s < s1; ++s) local += mla_parts(p, p.seq_lens[s]);
-  scan[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int v = tid >= off ? scan[tid - off] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
-  }
-  const int total = min(scan[1023], max_items);
+  int all;
+  int pos = block_exclusive_scan<1024>(local, warp_sums, &all);
+  const int total = min(all, max_items);
   const bool sort = total <= kMlaSortMax;
-  int pos = scan[tid] - local;
   for (int s = s0; s < s1; ++s) {
     const int L_raw = p.seq_lens[s];
     const int L = max(0, min(L_raw, p.cap));

@@ -164,7 +164,7 @@ constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const PrefillParams p, int4* items,
                                                                           int* count, int max_items) {
-  __shared__ int scan[kSchedThreads];
+  __shared__ int warp_sums[32];
   __shared__ int4 buf[kSortMax];
   pdl_launch_dependents();  // the attention kernel may start launching (it waits for the items)
   pdl_wait();  // a programmatic dependent itself: inputs are read once the previous grid completed
@@ -179,17 +179,10 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
     pf_lengths(p, s, L, q_len, routed);  // a routed decode's content errors are flagged here
     if (!routed) local += (q_len + pair_tokens - 1) / pair_tokens;
   }
-  scan[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < kSchedThreads; off <<= 1) {
-    const int v = tid >= off ? scan[tid - off] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
-  }
-  const int total = min(scan[kSchedThreads - 1], max_items);
+  int all;
+  int pos = block_exclusive_scan<kSchedThreads>(local, warp_sums, &all);
+  const int total = min(all, max_items);
   const bool sort = total <= kSortMax;
-  int pos = scan[tid] - local;
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
     pf_lengths(p, s, L, q_len, false);
