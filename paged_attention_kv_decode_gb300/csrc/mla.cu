@@ -633,63 +633,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       // (instead of 32 rows x 32 bytes).  Lane 4 q + i then holds chunk i of rows
       // 4 q .. 4 q + 3 of its warp's 32.
       const int gq = lane >> 2, gi = lane & 3;
-      auto transpose4 = [&](uint32_t* wv) {
+      auto transpose4 = [&](uint32_t* wv, const int cw) {  // chunks of cw words (8 or 4)
         const int b0 = lane & 1, b1 = (lane >> 1) & 1;
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t x = b0 ? wv[8 * (2 * sl) + k] : wv[8 * (2 * sl + 1) + k];
+            if (k >= cw) break;
+            const uint32_t x = b0 ? wv[cw * (2 * sl) + k] : wv[cw * (2 * sl + 1) + k];
             const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 1);
             if (b0)
-              wv[8 * (2 * sl) + k] = y;
+              wv[cw * (2 * sl) + k] = y;
             else
-              wv[8 * (2 * sl + 1) + k] = y;
+              wv[cw * (2 * sl + 1) + k] = y;
           }
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t x = b1 ? wv[8 * sl + k] : wv[8 * (2 + sl) + k];
+            if (k >= cw) break;
+            const uint32_t x = b1 ? wv[cw * sl + k] : wv[cw * (2 + sl) + k];
             const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 2);
             if (b1)
-              wv[8 * sl + k] = y;
+              wv[cw * sl + k] = y;
             else
-              wv[8 * (2 + sl) + k] = y;
+              wv[cw * (2 + sl) + k] = y;
           }
       };
+      // O leaves TMEM a block at a time: once a block is converted into wv, the next
+      // block's TMEM load is issued into the freed registers and stays in flight
+      // while wv is transposed and stored
       if (w.direct) {
-        // 64 bf16 columns (128 B) per row and step
+        // 32 bf16 columns (64 B) per row and block: 16-byte chunks, so a warp store
+        // writes 8 rows x 64 contiguous bytes
+        uint32_t ov[32], wv[16];
+        tmem_ld32(lane_base + kTmO, ov);
 #pragma unroll 1
-        for (int c64 = 0; c64 < kMlaHalf / 64; ++c64) {
-          uint32_t ov[64], wv[32];
-          tmem_ld32(lane_base + kTmO + c64 * 64, ov);
-          tmem_ld32(lane_base + kTmO + c64 * 64 + 32, ov + 32);
+        for (int c32 = 0; c32 < kMlaHalf / 32; ++c32) {
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < 16; ++j)
             wv[j] = pack_bf16x2(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
-          transpose4(wv);
+          if (c32 + 1 < kMlaHalf / 32) tmem_ld32(lane_base + kTmO + (c32 + 1) * 32, ov);
+          transpose4(wv, 4);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int rr = quarter * 32 + 4 * gq + c;  // the row this lane writes a chunk of
             const int hd = w.ht * kMlaRows + rr;
             if (rr < p.hrows && hd < p.H)
-              st_global_v8(reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)w.s * p.H + hd) * kMlaDv +
-                               rank * kMlaHalf + c64 * 64 + gi * 16,
-                           wv + 8 * c);
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)w.s * p.H + hd) * kMlaDv +
+                                        rank * kMlaHalf + c32 * 32 + gi * 8) =
+                  make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
           }
         }
       } else {
-        // 32 fp32 columns (128 B) per row and step
+        // 32 fp32 columns (128 B) per row and block
+        uint32_t ov[32], wv[32];
+        tmem_ld32(lane_base + kTmO, ov);
 #pragma unroll 1
         for (int c32 = 0; c32 < kMlaHalf / 32; ++c32) {
-          uint32_t wv[32];
-          tmem_ld32(lane_base + kTmO + c32 * 32, wv);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) wv[j] = __float_as_uint(__uint_as_float(wv[j]) * inv);
-          transpose4(wv);
+          for (int j = 0; j < 32; ++j) wv[j] = __float_as_uint(__uint_as_float(ov[j]) * inv);
+          if (c32 + 1 < kMlaHalf / 32) tmem_ld32(lane_base + kTmO + (c32 + 1) * 32, ov);
+          transpose4(wv, 8);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int rr = quarter * 32 + 4 * gq + c;
