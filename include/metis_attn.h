@@ -397,6 +397,25 @@ int metis_prefix_lookup(const uint64_t* keys, int n, uint64_t* table_keys, int32
                         uint8_t* hits_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * metis_debug_wait_probe -- test support for the bounded waits.
+ *
+ * Every pipeline wait in the library (an mbarrier phase a producer or the
+ * tensor cores complete) gives up after a time limit instead of spinning
+ * forever: it sets METIS_STATUS_WAIT_TIMEOUT in the device status word and the
+ * kernel returns, so a library bug surfaces as a status bit and the CUDA
+ * context stays usable.  This call runs that give-up path on purpose: it
+ * launches one warp whose wait on an mbarrier can never complete (the barrier
+ * expects an arrival that never comes), bounded by limit_ns nanoseconds.
+ *
+ *   limit_ns   (0, 1e9]: the wait's wall-time limit; otherwise METIS_E_SHAPE
+ *              and nothing is launched
+ *
+ * Asynchronous on `stream`; afterwards metis_read_status() reports
+ * METIS_STATUS_WAIT_TIMEOUT.  Not part of any attention path.
+ */
+int metis_debug_wait_probe(uint64_t limit_ns, void* stream);
+
+/*
  * metis_read_status -- the device status word (METIS_STATUS_* bits, OR-ed
  * over every launch since it was last cleared) of the current device.
  * Synchronises the device: for tests and debugging, not for the hot path.

@@ -40,6 +40,7 @@ from ._binding import (  # noqa: F401
     prefix_table_alloc,
     split_workspace_views,
     metis_read_status,
+    metis_debug_wait_probe,
     metis_reshape_and_cache,
     metis_version,
 )

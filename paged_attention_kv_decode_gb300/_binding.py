@@ -81,6 +81,7 @@ SIGNATURES = {
     "metis_prefix_table_init": (_i, [_vp, _vp, _vp, _i, _vp]),
     "metis_prefix_lookup_workspace_bytes": (_sz, [_i]),
     "metis_prefix_lookup": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+    "metis_debug_wait_probe": (_i, [ctypes.c_uint64, _vp]),
 }
 
 
@@ -499,3 +500,8 @@ def metis_prefix_lookup(keys: torch.Tensor, table, free_stack: torch.Tensor, fre
                                    refcount.shape[0], _ptr(pages_out), _ptr(hits_out), _ptr(workspace),
                                    workspace.numel(), _stream(stream)))
     return pages_out, hits_out
+
+
+def metis_debug_wait_probe(limit_ns: int, stream=None) -> None:
+    """Run the bounded-wait give-up path once (a wait that nothing completes, limited to limit_ns)."""
+    _check(load_library().metis_debug_wait_probe(int(limit_ns), _stream(stream)))

@@ -71,6 +71,20 @@ __global__ void __launch_bounds__(128) mla_reshape_and_cache_kernel(const uint4*
     d[i] = i < lat_vecs ? __ldg(kv_c + (size_t)n * lat_vecs + i) : __ldg(k_pe + (size_t)n * rope_vecs + (i - lat_vecs));
 }
 
+// Test support: an mbarrier wait that nothing can complete (the barrier expects
+// one arrival that never comes), bounded by limit_ns: the wait gives up, sets
+// METIS_STATUS_WAIT_TIMEOUT and the kernel returns.  This is the give-up path of
+// every pipeline wait in the library, run on purpose.
+__global__ void __launch_bounds__(32) wait_probe_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait_for(&bar, 0, &g_status_cache, limit_ns);
+}
+
 int cache_status(uint32_t* bits, int clear) {
   unsigned int v = 0;
   cudaError_t e = cudaDeviceSynchronize();
@@ -134,4 +148,12 @@ extern "C" int metis_mla_reshape_and_cache(const void* kv_c, const void* k_pe, v
       reinterpret_cast<const uint4*>(kv_c), reinterpret_cast<const uint4*>(k_pe), reinterpret_cast<uint4*>(kv_cache),
       slot_mapping, lat_vecs, rope_vecs, (long long)num_blocks * block_size);
   return check_launch("mla_reshape_and_cache_kernel launch");
+}
+
+extern "C" int metis_debug_wait_probe(uint64_t limit_ns, void* stream) {
+  clear_error();
+  if (limit_ns == 0 || limit_ns > 1000000000ull)
+    return fail(METIS_E_SHAPE, "limit_ns must be in (0, 1e9]");
+  wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+  return check_launch("wait_probe_kernel launch");
 }

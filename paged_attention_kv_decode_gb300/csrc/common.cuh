@@ -97,17 +97,23 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 constexpr uint32_t kMaxPolls = 1u << 26;
 constexpr uint64_t kMaxWaitNs = 2000000000ull;
 
-// Wait for the phase with the given parity to complete.  Returns false (and
-// sets the timeout bit in *status) if it does not complete in time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+// Wait for the phase with the given parity to complete, for at most limit_ns of
+// wall time (and kMaxPolls polls).  Returns false (and sets the timeout bit in
+// *status) if it does not complete in time.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < kMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 0 && global_timer_ns() - t0 > kMaxWaitNs) break;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) break;
   }
   atomicOr(status, METIS_STATUS_WAIT_TIMEOUT);
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+  return mbar_wait_for(bar, parity, status, kMaxWaitNs);
 }
 
 // ---------------------------------------------------------------------------

@@ -270,3 +270,9 @@ def test_prefix_lookup_empty_and_workspace(lib):
     assert lib.metis_prefix_lookup(None, 0, None, None, None, 0, None, 0, None, None, 0, None, None, None, 0, None) == 0
     assert lib.metis_prefix_lookup_workspace_bytes(0) == 0
     assert lib.metis_prefix_lookup_workspace_bytes(16) >= 16 * 5
+
+
+@pytest.mark.parametrize("limit_ns", [0, 1_000_000_001, 2 ** 63])
+def test_wait_probe_rejects_limits_outside_one_second(lib, limit_ns):
+    assert lib.metis_debug_wait_probe(limit_ns, None) == -2   # METIS_E_SHAPE
+    assert "limit_ns" in pa.metis_last_error()
