@@ -91,6 +91,7 @@ constexpr int kMlaSortMax = 2048;
 constexpr int kMlaStages = 4;       // TMA ring stages (one unit each)
 constexpr float kMlaSlack = 8.0f;   // a unit keeps a published reference while its maximum is within 2^8 of it
 constexpr int kMlaWorkCache = 256;  // works per cluster kept in shared memory (beyond: read from the list)
+constexpr int kMlaInlineSeqs = 512;  // batches up to this many sequences are ranked inside the kernel
 constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
 constexpr uint32_t kTmS = 256;      // 2 x 64 columns: partial scores of the units of set 0 / set 1
 constexpr uint32_t kTmQ = 384;      // 128 columns: latent part of Q_r as bf16 pairs
@@ -143,13 +144,15 @@ struct MlaParams {
   int S, H, hrows, head_tiles, bs, max_blocks, num_blocks, cap, P, max_parts;
   int box_rows;     // rows per TMA box (a divisor of the unit that never crosses a page)
   float scale_log2;
+  int inline_list;  // 1: each CTA ranks its own works (no schedule kernel, items / item_count unused)
 };
 
 // partitions of sequence s: the merge reads ceil(L / P) of them (at most max_parts)
-__device__ __forceinline__ int mla_parts(const MlaParams& p, int L_raw) {
-  if (p.P <= 0) return 1;
-  return max(1, min(L_raw / p.P + (L_raw % p.P != 0), p.max_parts));   // ceil without overflow
+__device__ __forceinline__ int mla_parts_of(int P, int max_parts, int L_raw) {
+  if (P <= 0) return 1;
+  return max(1, min(L_raw / P + (L_raw % P != 0), max_parts));   // ceil without overflow
 }
+__device__ __forceinline__ int mla_parts(const MlaParams& p, int L_raw) { return mla_parts_of(p.P, p.max_parts, L_raw); }
 
 __global__ void __launch_bounds__(1024) mla_schedule_kernel(const MlaParams p, int4* items, int* count,
                                                             int max_items) {
@@ -230,6 +233,67 @@ __device__ __forceinline__ MlaWork mla_work_decode(const MlaParams& p, int4 raw)
   return w;
 }
 
+// Small batches: the works of cluster cl of G, ranked by every CTA itself instead
+// of by a schedule kernel.  The list is every (sequence, partition) ordered by
+// tokens, heaviest first, ties in (sequence, partition) order -- the schedule
+// kernel's order -- times the head tiles.  A sequence's partitions are `full` of P
+// tokens, then at most one partial one (0 < rem < P tokens), then empty ones, so
+// the list is: every full partition in sequence order (a prefix sum), the partial
+// ones by rem (a count over the sequences), every empty one in sequence order (a
+// prefix sum).  Without a split each sequence is one "partial" partition of all
+// its tokens.  Thread t ranks sequence t (S <= the block size); sWorks[r] receives
+// the work at the cluster's r-th snake position.  `scratch` holds kMlaInlineSeqs +
+// 32 ints.  Returns the number of works (items x head tiles); the list has fewer
+// than 2^15 items.
+__device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_lens, int S, int P, int cap,
+                                               int max_parts, int head_tiles, int* scratch, int4* sWorks, int cl,
+                                               int G) {
+  int* sRem = scratch;                      // [S] tokens of the partial partition (0: none)
+  int* sWarp = scratch + kMlaInlineSeqs;    // scan scratch
+  const int sq = threadIdx.x;
+  int np = 0, full = 0, has = 0, rem = 0, Lr = 0;
+  if (sq < S) {
+    Lr = seq_lens[sq];
+    const int Lc = max(0, min(Lr, cap));
+    np = mla_parts_of(P, max_parts, Lr);
+    if (P <= 0) {
+      has = 1;
+      rem = Lc;
+    } else {
+      full = min(np, Lc / P);
+      rem = full < np ? Lc - full * P : 0;
+      has = rem > 0;
+    }
+    sRem[sq] = rem;
+  }
+  const int empty = np - full - has;
+  // full and empty counts packed in one scan (each list total is below 2^15)
+  int tot;
+  const int before = block_exclusive_scan<kMlaThreads>(full | (empty << 16), sWarp, &tot);
+  const int n_partial = __syncthreads_count(has);
+  const int F = tot & 0xffff, E = tot >> 16;
+  const int n_work = (F + n_partial + E) * head_tiles;
+  if (cl >= n_work) return n_work;
+  int partial_rank = F;
+  if (has) {
+    for (int t = 0; t < S; ++t) {
+      const int r2 = sRem[t];
+      partial_rank += (r2 > rem) || (r2 == rem && t < sq);
+    }
+  }
+  for (int q = 0; q < np; ++q) {
+    const int rank = q < full ? (before & 0xffff) + q
+                     : (q == full && has) ? partial_rank
+                                          : F + n_partial + (before >> 16) + (q - full - has);
+    for (int ht = 0; ht < head_tiles; ++ht) {
+      const int pos = rank * head_tiles + ht;
+      const int row = pos / G, col = pos - row * G;
+      if (((row & 1) ? G - 1 - col : col) == cl) sWorks[row] = make_int4(sq, q, ht, Lr);
+    }
+  }
+  return n_work;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKVh,
                       const MlaParams p) {
@@ -267,21 +331,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
   const uint32_t peer = rank ^ 1u;
   const int cl = blockIdx.x >> 1, G = gridDim.x >> 1;
-  const int n_work = *p.item_count * p.head_tiles;
-  if (cl >= n_work) return;  // both CTAs of the cluster take the same branch
   // The cluster's works, cached in shared memory (every role walks the same list;
   // the units of all works are numbered g = 0, 1, ...).
   int4* sWorks = reinterpret_cast<int4*>(smem + Sh::kWorks);
-  int* sCount = reinterpret_cast<int*>(bars + MlaBar::kCount + 2);
+  int* sCount = reinterpret_cast<int*>(bars + MlaBar::kCount + 2);  // [0] units of the cluster, [1] works
   if (threadIdx.x == 0) sCount[0] = 0;
-  __syncthreads();
+  int n_work;
   int my_units = 0;
-  for (int r = threadIdx.x; r < kMlaWorkCache; r += kMlaThreads) {
-    const long long pos = mla_work_pos(cl, G, r);
-    if (pos >= n_work) break;
-    const int4 raw = mla_work_raw(p, pos);
-    sWorks[r] = raw;
-    my_units += mla_work_decode(p, raw).n_units;
+  if (p.inline_list) {
+    const int nw = mla_rank_inline(p.seq_lens, p.S, p.P, p.cap, p.max_parts, p.head_tiles,
+                                   reinterpret_cast<int*>(sSlot), sWorks, cl, G);
+    // read back from shared memory: a value the compiler sees as uniform (a
+    // per-thread copy would hold a register through every role below)
+    if (threadIdx.x == 0) sCount[1] = nw;
+    __syncthreads();
+    n_work = sCount[1];
+    if (cl >= n_work) return;  // both CTAs of the cluster take the same branch
+    __syncthreads();
+    for (int r = threadIdx.x; r < kMlaWorkCache; r += kMlaThreads) {
+      if (mla_work_pos(cl, G, r) >= n_work) break;
+      my_units += mla_work_decode(p, sWorks[r]).n_units;
+    }
+  } else {
+    n_work = *p.item_count * p.head_tiles;
+    if (cl >= n_work) return;  // both CTAs of the cluster take the same branch
+    __syncthreads();
+    for (int r = threadIdx.x; r < kMlaWorkCache; r += kMlaThreads) {
+      const long long pos = mla_work_pos(cl, G, r);
+      if (pos >= n_work) break;
+      const int4 raw = mla_work_raw(p, pos);
+      sWorks[r] = raw;
+      my_units += mla_work_decode(p, raw).n_units;
+    }
   }
   atomicAdd(sCount, my_units);
   __syncthreads();
@@ -984,10 +1065,25 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
                     CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
 
-  // a programmatic dependent of the kernel before it (e.g. the latent-cache write)
-  rc = launch_dependent(mla_schedule_kernel, dim3(1), dim3(1024), 0, st, "mla_schedule_kernel launch", p, items, count,
-                        (int)lay.max_items);
-  if (rc) return rc;
+  // persistent: one cluster (two SMs) per SM pair, each walking its share of the work list
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return fail(METIS_E_CUDA, "SM count: %s", cudaGetErrorString(ce));
+  const size_t clusters = std::max<size_t>(1, std::min<size_t>((size_t)(sms / 2), lay.max_items * head_tiles));
+  // Small batches: every CTA ranks its own works (no schedule kernel on the critical
+  // path); otherwise a schedule kernel lists them, heaviest first.
+  p.inline_list = num_seqs <= kMlaInlineSeqs && lay.max_items < 32768 &&
+                  lay.max_items * head_tiles <= (size_t)kMlaWorkCache * clusters;
+#ifdef METIS_MLA_NO_INLINE
+  p.inline_list = 0;
+#endif
+  if (!p.inline_list) {
+    // a programmatic dependent of the kernel before it (e.g. the latent-cache write)
+    rc = launch_dependent(mla_schedule_kernel, dim3(1), dim3(1024), 0, st, "mla_schedule_kernel launch", p, items,
+                          count, (int)lay.max_items);
+    if (rc) return rc;
+  }
   static int done = 0;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), MlaShape::kSmem, &done);
   if (rc) return rc;
@@ -1003,12 +1099,6 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
                   (2 * kMlaRegsRow + 2 * kMlaRegsLow) / 4);
     regs_checked = 1;
   }
-  // persistent: one cluster (two SMs) per SM pair, each walking its share of the work list
-  int dev = 0, sms = 0;
-  cudaError_t ce = cudaGetDevice(&dev);
-  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (ce != cudaSuccess) return fail(METIS_E_CUDA, "SM count: %s", cudaGetErrorString(ce));
-  const size_t clusters = std::max<size_t>(1, std::min<size_t>((size_t)(sms / 2), lay.max_items * head_tiles));
   rc = launch_dependent(mla_decode_kernel, dim3((unsigned)(clusters * 2)), dim3(kMlaThreads), MlaShape::kSmem, st,
                         "mla_decode_kernel launch", tmKV, tmKVh, p);
   if (rc) return rc;
