@@ -244,6 +244,9 @@ size_t metis_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads
  * operands, fp32 accumulation.  Persistent clusters of two CTAs (two SMs), one
  * per SM pair, split the key dimensions and the output columns of each work
  * item (a sequence, or a partition of one) and walk their share of the items.
+ * The two halves of each score (288 key dimensions each, accumulated in fp32)
+ * are scaled by scale * log2(e) and rounded to fp16 before they are added, so a
+ * score carries an extra error of at most 2^-11 (|S_0| + |S_1|) in log2 units.
  */
 int metis_mla_decode(const void* q, const void* kv_cache,
                      const int32_t* block_table, const int32_t* seq_lens,

@@ -14,13 +14,16 @@
 //   * scores: CTA r owns the key dimensions D_r = [256 r, 256 r + 256) of the
 //     latent part plus [512 + 32 r, 512 + 32 r + 32) of the rope part and
 //     computes the partial S_r = Q[:, D_r] K[:, D_r]^T for all 128 heads;
-//   * ONE exchange per 64-token unit: each CTA stores its partial scores of
-//     all heads straight into the peer's shared memory (asynchronous
-//     distributed-shared-memory stores that count their bytes on the peer's
-//     barrier, which the peer armed with the 32 KB it awaits), so both
-//     CTAs form the full S = S_0 + S_1 (fp32 addition commutes: both get the
-//     same bits) and both run the softmax of every head -- no probabilities
-//     travel back;
+//   * ONE exchange per 64-token unit: each CTA scales its partial scores of all
+//     heads into the log2 domain, rounds them to fp16 and stores them straight
+//     into the peer's shared memory (asynchronous distributed-shared-memory
+//     stores that count their bytes on the peer's barrier, which the peer armed
+//     with the 16 KB it awaits); both CTAs form S = f16(S_0) + f16(S_1) in fp32
+//     (addition commutes: both get the same bits) and both run the softmax of
+//     every head -- no probabilities travel back.  The rounding moves a score by
+//     at most 2^-11 (|S_0| + |S_1|), below the bf16 rounding that the queries and
+//     the latent carry (2^-9 each), and halves the slots, which buys the ring
+//     its fifth stage;
 //   * output: CTA r owns output columns [256 r, 256 r + 256) (O_r in TMEM), whose
 //     values are exactly the latent columns it already loads for its keys.
 //
@@ -37,17 +40,17 @@
 // 2^(C - c) (after the previous P V completes); c < C scales the unit's P rows
 // by 2^(c - C) instead (never O up, which could overflow); c = C costs nothing.
 //
-// Per 64-token unit and CTA: 36 KB of latent through a 4-stage TMA ring (four
+// Per 64-token unit and CTA: 36 KB of latent through a 5-stage TMA ring (four
 // 128-byte-swizzled 64-column blocks and one 64-byte-swizzled 32-column rope
 // block); the score UMMA is M 128 x N 64 x K 288 (Q_r's latent part from TMEM,
 // its rope part from shared memory); P V is M 128 x N 256 x K 64.  The unit's
-// 32 KB exchange slot first receives the peer's partial scores, then holds P
+// 16 KB exchange slot first receives the peer's partial scores, then holds P
 // (the peer writes the slot again only after P V of the unit completed, which
 // the UMMA warp signals to it with a multicast commit).  The slot is laid out
-// per row warp: warp w's 32 heads own bytes [8 KB w, 8 KB (w + 1)), the scores
+// per row warp: warp w's 32 heads own bytes [4 KB w, 4 KB (w + 1)), the scores
 // as [16-byte chunk][lane] (so one warp-wide store or load is 512 contiguous
-// bytes, also across the cluster), and P's 128-byte-swizzled rows in 8-row
-// groups 2 KB apart, so the P rows of warp w fall inside warp w's own scores:
+// bytes, also across the cluster), and P's 128-byte-swizzled rows in dense 8-row
+// groups (1 KB apart), so the P rows of warp w fall exactly on warp w's own scores:
 // a warp overwrites what it has just read and needs no other warp.
 //
 // TMEM (512 columns): O_r 256 | S 2 x 64 | Q_r's latent part as bf16 pairs 128.
@@ -88,9 +91,9 @@ constexpr int kMlaRegsLow = 112;    // warpgroups 2 and 3: rescale, TMA, UMMA
 static_assert(128 * (2 * kMlaRegsRow + 2 * kMlaRegsLow) <= 65536, "register split exceeds the register file");
 constexpr int kMlaTmemCols = 512;
 constexpr int kMlaSortMax = 2048;
-constexpr int kMlaStages = 4;       // TMA ring stages (one unit each)
+constexpr int kMlaStages = 5;       // TMA ring stages (one unit each)
 constexpr float kMlaSlack = 8.0f;   // a unit keeps a published reference while its maximum is within 2^8 of it
-constexpr int kMlaWorkCache = 256;  // works per cluster kept in shared memory (beyond: read from the list)
+constexpr int kMlaWorkCache = 128;  // works per cluster kept in shared memory (beyond: read from the list)
 constexpr int kMlaInlineSeqs = 512;  // batches up to this many sequences are ranked inside the kernel
 constexpr uint32_t kTmO = 0;        // 256 fp32 columns: O_r
 constexpr uint32_t kTmS = 256;      // 2 x 64 columns: partial scores of the units of set 0 / set 1
@@ -100,9 +103,9 @@ struct MlaShape {
   static constexpr int kBlk = kMlaUnit * 128;             // one 64-column block of a unit (128-byte rows)
   static constexpr int kStage = 4 * kBlk;                 // the unit's latent columns of this CTA
   static constexpr int kRopeU = kMlaUnit * 64;            // the unit's rope half block (64-byte rows)
-  static constexpr int kSlotB = kMlaRows * kMlaUnit * 4;  // exchange slot: fp32 partial scores, later bf16 P
+  static constexpr int kSlotB = kMlaRows * kMlaUnit * 2;  // exchange slot: fp16 partial scores, later bf16 P
   static constexpr int kWarpB = kSlotB / 4;               // a row warp's part of the slot
-  static constexpr int kPGroup = 2048;                    // P: bytes between 8-row groups
+  static constexpr int kPGroup = 1024;                    // P: bytes between 8-row groups
   static constexpr int kKv = 0;                           // stage s at kKv + s * kStage, block b at + b * kBlk
   static constexpr int kRope = kKv + kMlaStages * kStage; // stage s at kRope + s * kRopeU
   static constexpr int kSlot = kRope + kMlaStages * kRopeU;  // slot k (units of set k) at kSlot + k * kSlotB
@@ -816,7 +819,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     uint8_t* prow = my_slot + (hr >> 3) * Sh::kPGroup + (hr & 7) * 128;   // inside this warp's part
     const int sw8 = hr & 7;
     const float sl2 = p.scale_log2;
-    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     bool ok = true;
     int g0 = 0;  // first unit of the current work
     MlaWork w;
@@ -857,9 +859,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           ok = false;
           break;
         }
+        // this CTA's partial in the log2 domain, rounded to fp16 (saturating): what
+        // travels, and what this CTA adds, so that both CTAs hold the same sums
+        uint32_t hv[kMlaUnit / 2];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          st_async_v4(peer_part + j * 512, sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3], peer_rx_full);
+        for (int j = 0; j < kMlaUnit / 2; ++j)
+          hv[j] = pack_f16x2_sat(__uint_as_float(sv[2 * j]) * sl2, __uint_as_float(sv[2 * j + 1]) * sl2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_async_v4(peer_part + j * 512, hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3], peer_rx_full);
         // the peer's partial of the same unit, in this CTA's slot
         if (!wait_all(&rx_full[set], ph)) {
           ok = false;
@@ -868,17 +876,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         // expect the peer's partial of this set's next unit (it can only come after
         // this unit's P V, which follows everything below)
         if (quarter == 0 && lane == 0 && g + 2 < g_total) mbar_arrive_expect_tx(&rx_full[set], Sh::kSlotB);
-        // full scores, scaled into the log2 domain: x = (own + peer) * scale * log2(e)
+        // full scores in the log2 domain: x = own + peer (fp32 sum of the fp16 partials)
         float x[kMlaUnit];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float4 r4 = *reinterpret_cast<const float4*>(rx_part + j * 512);
-          const uint64_t a = f2_mul(f2_add(f2_pack(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])),
-                                           f2_pack(r4.x, r4.y)), sl2x2);
-          const uint64_t b = f2_mul(f2_add(f2_pack(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])),
-                                           f2_pack(r4.z, r4.w)), sl2x2);
-          f2_unpack(a, x[4 * j], x[4 * j + 1]);
-          f2_unpack(b, x[4 * j + 2], x[4 * j + 3]);
+        for (int j = 0; j < 8; ++j) {
+          const uint4 r4 = *reinterpret_cast<const uint4*>(rx_part + j * 512);
+          const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 a = unpack_f16x2(hv[4 * j + i]);
+            const float2 b = unpack_f16x2(rw[i]);
+            f2_unpack(f2_add(f2_pack(a.x, a.y), f2_pack(b.x, b.y)), x[8 * j + 2 * i], x[8 * j + 2 * i + 1]);
+          }
         }
         __syncwarp();  // the warp's scores are read before its P overwrites them
         const int vis = min(kMlaUnit, w.t1 - (w.t0 + u * kMlaUnit));

@@ -6,7 +6,8 @@ import torch
 # Tolerances of the parity bar: fp32 max |d| <= 1e-5; bf16 inputs with fp32
 # accumulation |d| <= 1.5e-2 + 1e-2 |ref| elementwise.  lse (always fp32) of a
 # bf16 case is held to 1e-3 absolute: it only sees fp32 rounding of exact
-# bf16 products.
+# bf16 products -- except in MLA decode, whose two CTAs exchange partial scores
+# as fp16; its tests add that rounding's bound per row (assert_lse's `extra`).
 F32_ATOL = 1e-5
 BF16_ATOL = 1.5e-2
 BF16_RTOL = 1e-2
@@ -36,15 +37,21 @@ def assert_parity(got: torch.Tensor, ref: np.ndarray, dtype: torch.dtype, what: 
     return float(d.max())
 
 
-def assert_lse(got: torch.Tensor, ref: np.ndarray, dtype: torch.dtype):
+def assert_lse(got: torch.Tensor, ref: np.ndarray, dtype: torch.dtype, extra: np.ndarray = None):
+    """lse against the oracle; `extra` (shaped like ref) adds a per-element bound for
+    a rounding step that the kernel takes on purpose (the MLA score exchange)."""
     g = f64(got)
     fin = np.isfinite(ref)
     assert np.array_equal(np.isfinite(g), fin), "lse: -inf pattern differs"
     assert (g[~fin] == ref[~fin]).all()
-    tol = F32_ATOL if dtype == torch.float32 else BF16_LSE_ATOL
+    tol = np.full(ref.shape, F32_ATOL if dtype == torch.float32 else BF16_LSE_ATOL)
+    if extra is not None:
+        tol = tol + extra
     if fin.any():
-        d = np.abs(g[fin] - ref[fin]).max()
-        assert d <= tol, f"lse: max abs err {d:.3e} > {tol}"
+        d = np.zeros(ref.shape)
+        d[fin] = np.abs(g[fin] - ref[fin])
+        worst = np.unravel_index(np.argmax(d - tol), d.shape)
+        assert (d <= tol).all(), f"lse: max abs err {d.max():.3e}; at {worst} {d[worst]:.3e} > {tol[worst]:.3e}"
 
 
 def replace_blocks(k_cache, v_cache, block_table, seq_lens, seed):
