@@ -165,6 +165,13 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
                : "memory");
 }
 
+// 32-byte read-only global load (8 words; the address 32-byte aligned)
+__device__ __forceinline__ void ld_global_nc_v8(const void* ptr, uint32_t* v) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(ptr));
+}
+
 // ---------------------------------------------------------------------------
 // warp-level matrix helpers (bf16)
 // ---------------------------------------------------------------------------

@@ -147,6 +147,7 @@ struct MlaParams {
   int S, H, hrows, head_tiles, bs, max_blocks, num_blocks, cap, P, max_parts;
   int box_rows;     // rows per TMA box (a divisor of the unit that never crosses a page)
   float scale_log2;
+  int q_v8;         // 1: q is 32-byte aligned (its rows are read in 32-byte pieces), else 16-byte pieces
   int inline_list;  // 1: each CTA ranks its own works (no schedule kernel, items / item_count unused)
 };
 
@@ -432,12 +433,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool row_valid;
     const uint4* src = q_row(w, hr, row_valid);
-    for (int c0 = 0; c0 < 128; c0 += 64) {  // two rounds of 16 loads (the row is 36 chunks; rope last)
+    for (int c0 = 0; c0 < 128; c0 += 64) {  // two rounds of 256 B of the row's latent half (rope last)
       uint32_t v[64];
+      if (p.q_v8) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint4 x4 = row_valid ? __ldg(src + 32 * rank + c0 / 4 + i) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * i] = x4.x, v[4 * i + 1] = x4.y, v[4 * i + 2] = x4.z, v[4 * i + 3] = x4.w;
+        for (int i = 0; i < 8; ++i) {
+          if (row_valid)
+            ld_global_nc_v8(src + 32 * rank + c0 / 4 + 2 * i, v + 8 * i);
+          else
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[8 * i + k] = 0u;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 x4 = row_valid ? __ldg(src + 32 * rank + c0 / 4 + i) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * i] = x4.x, v[4 * i + 1] = x4.y, v[4 * i + 2] = x4.z, v[4 * i + 3] = x4.w;
+        }
       }
       tmem_st32(lane_base + kTmQ + c0, v);
       tmem_st32(lane_base + kTmQ + c0 + 32, v + 32);
@@ -1062,6 +1074,7 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
 
   // 64-row boxes (fewer, larger TMA copies) when every unit starts on a multiple of 64 tokens
   p.box_rows = std::min(block_size, (partition_size % kMlaUnit == 0) ? kMlaUnit : kMlaAlign);
+  p.q_v8 = aligned(q, 32);
   CUtensorMap tmKV, tmKVh;
   const uint64_t kdims[3] = {(uint64_t)kMlaDq, 1, (uint64_t)num_blocks * block_size};
   const uint64_t kstr[2] = {(uint64_t)kMlaDq * 2, (uint64_t)kMlaDq * 2};

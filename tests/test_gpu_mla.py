@@ -130,6 +130,22 @@ def test_mla_full_size_every_output():
     assert_lse(lse, ref_l, torch.bfloat16, exchange_bound(case))
 
 
+def test_queries_only_16_byte_aligned():
+    """q that starts 16 bytes past a 32-byte boundary takes the 16-byte row loads: same results bitwise."""
+    case = wl.make_mla_case(87, [1, 64, 200, 700], H=128, bs=64)
+    base, base_lse = gpu_mla(case, 256)
+    n = case.q.numel()
+    buf = torch.empty(n + 8, dtype=case.q.dtype, device="cuda")
+    q16 = buf[8:].view(case.q.shape)
+    q16.copy_(dev(case.q))
+    assert q16.data_ptr() % 32 == 16
+    out, lse = pa.metis_mla_decode(q16, dev(case.kv_cache), dev(case.block_table), dev(case.seq_lens), case.scale,
+                                   partition_size=256, max_seq_len=case.max_seq_len, want_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, base) and torch.equal(lse, base_lse)
+    assert pa.metis_read_status() == 0
+
+
 def test_bad_block_id_is_flagged():
     case = wl.make_mla_case(85, [130, 90], H=128, bs=64)
     bt = case.block_table.clone()
