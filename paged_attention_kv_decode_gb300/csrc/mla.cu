@@ -1097,9 +1097,6 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
   // path); otherwise a schedule kernel lists them, heaviest first.
   p.inline_list = num_seqs <= kMlaInlineSeqs && lay.max_items < 32768 &&
                   lay.max_items * head_tiles <= (size_t)kMlaWorkCache * clusters;
-#ifdef METIS_MLA_NO_INLINE
-  p.inline_list = 0;
-#endif
   if (!p.inline_list) {
     // a programmatic dependent of the kernel before it (e.g. the latent-cache write)
     rc = launch_dependent(mla_schedule_kernel, dim3(1), dim3(1024), 0, st, "mla_schedule_kernel launch", p, items,
