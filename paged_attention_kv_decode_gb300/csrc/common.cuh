@@ -165,6 +165,12 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
                : "memory");
 }
 
+// Barrier over nthreads threads (whole warps) of the block on hardware barrier id
+// (1..15; id 0 is __syncthreads').
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // 32-byte read-only global load (8 words; the address 32-byte aligned)
 __device__ __forceinline__ void ld_global_nc_v8(const void* ptr, uint32_t* v) {
   asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"

@@ -65,13 +65,14 @@ __device__ __forceinline__ int decode_row(const DecodeParams& p, int s) {
 // Token range of this CTA, after clamping the sequence length.  Returns
 // false when the CTA has nothing to do (after writing what an empty
 // partition or sequence must leave behind).
+// tid / nthr: this thread's index among the threads that share the item.
 template <typename OutT>
 __device__ __forceinline__ bool decode_range(const DecodeParams& p, int part, int g, int s, int orow, int& t0,
-                                             int& t1) {
+                                             int& t1, int tid, int nthr) {
   int L_raw = p.seq_lens[s];
   int L = L_raw;
   if (L > p.cap) {
-    if (threadIdx.x == 0) atomicOr(&g_status_decode, METIS_STATUS_SEQ_TOO_LONG);
+    if (tid == 0) atomicOr(&g_status_decode, METIS_STATUS_SEQ_TOO_LONG);
     L = p.cap;
   }
   if (L < 0) L = 0;
@@ -85,12 +86,12 @@ __device__ __forceinline__ bool decode_range(const DecodeParams& p, int part, in
   if (t1 > t0) return true;
   if (p.partition_size > 0) {
     // A partition the merge will look at but that holds no readable token.
-    if (L_raw > 0 && t0 < L_raw && threadIdx.x < p.r)
-      p.part_lse[((size_t)s * p.H + g * p.r + threadIdx.x) * p.max_parts + part] = -INFINITY;
+    if (L_raw > 0 && t0 < L_raw && tid < p.r)
+      p.part_lse[((size_t)s * p.H + g * p.r + tid) * p.max_parts + part] = -INFINITY;
   } else {
     OutT* o = reinterpret_cast<OutT*>(p.out) + ((size_t)orow * p.H + (size_t)g * p.r) * p.D;
-    for (int i = threadIdx.x; i < p.r * p.D; i += blockDim.x) o[i] = OutT(0.0f);
-    if (p.lse_out && threadIdx.x < p.r) p.lse_out[(size_t)orow * p.H + g * p.r + threadIdx.x] = -INFINITY;
+    for (int i = tid; i < p.r * p.D; i += nthr) o[i] = OutT(0.0f);
+    if (p.lse_out && tid < p.r) p.lse_out[(size_t)orow * p.H + g * p.r + tid] = -INFINITY;
   }
   return false;
 }
@@ -117,10 +118,10 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 // split-KV partial.
 template <typename OutT, int NW>
 __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const float* cm, const float* cl,
-                                                  const float* co, int part, int g, int s, int orow) {
+                                                  const float* co, int part, int g, int s, int orow, int tid) {
   const int D = p.D;
   const int nq = D / 4;
-  for (int idx = threadIdx.x; idx < p.r * nq; idx += NW * 32) {
+  for (int idx = tid; idx < p.r * nq; idx += NW * 32) {
     const int h = idx / nq;
     const int d = (idx - h * nq) * 4;
     float M = -INFINITY;
@@ -196,42 +197,22 @@ __device__ __forceinline__ int seq_of_rank(const DecodeParams& p, int rank, int*
   return *found;
 }
 
-template <int D, int NW, int STAGES>
-__global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                               const __grid_constant__ CUtensorMap tmV,
-                                                               const DecodeParams p) {
+// One work item of the bf16 decode: the tokens [t0, t1) of KV head g of sequence s
+// (query / output row orow), run by NW warps (warp 0 .. NW - 1 of the caller's
+// group; tid = the thread's index in the group) over their NW x STAGES TMA ring at
+// smem with its barriers at bars.  kb: this warp's ring position before the item
+// (ring stages and barrier phases run on across the items of a persistent group),
+// advanced past the item's units.  sync(): a barrier over the group's threads.
+// The combine step reuses the ring: the caller syncs the group before the next
+// item's loads.  Returns false when a wait gave up.
+template <int D, int NW, int STAGES, typename Sync>
+__device__ __forceinline__ bool decode_bf16_item(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
+                                                 uint8_t* smem, uint64_t* bars, int part, int g, int s, int orow,
+                                                 int t0, int t1, int warp, int lane, int tid, int& kb, Sync sync) {
   using Shape = Bf16DecodeShape<D>;
   constexpr int HALVES = Shape::kHalves;
   constexpr int STAGE_BYTES = Shape::kStageBytes;
   constexpr int KS = Shape::kSteps;
-  static_assert(NW * (64 + D * 32) <= NW * STAGES * STAGE_BYTES, "combine area must fit in the ring");
-  pdl_launch_dependents();  // the merge may start launching; it waits for this grid to finish
-  // Launched as a programmatic dependent (e.g. of the paged K/V write): every input
-  // is read after the previous grid in the stream has completed.
-  pdl_wait();
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * STAGES * STAGE_BYTES);
-
-  __shared__ int rank_lens[kMaxRankSeqs];
-  __shared__ int rank_found;
-  const int part = blockIdx.x, g = blockIdx.y;
-  const int s = (p.partition_size == 0 && p.S <= kMaxRankSeqs) ? seq_of_rank(p, blockIdx.z, rank_lens, &rank_found)
-                                                                : (int)blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int orow = decode_row(p, s);
-  if (orow < 0) return;  // not a decode of this mixed batch
-  int t0, t1;
-  if (!decode_range<__nv_bfloat16>(p, part, g, s, orow, t0, t1)) return;
-
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    for (int i = 0; i < NW * STAGES; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
 
   // this warp's units: u0 + warp + k * NW, k < n_my
   const int u0 = t0 / kUnit;
@@ -258,7 +239,7 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
       win_next = row_coord(k + 32 + lane);
     }
     const int row = __shfl_sync(0xffffffffu, win_cur, k & 31);
-    const int st = k % STAGES;
+    const int st = (kb + k) % STAGES;
     uint8_t* base = smem + (warp * STAGES + st) * STAGE_BYTES;
     uint64_t* bar = &bars[warp * STAGES + st];
     if (lane == 0) mbar_arrive_expect_tx(bar, STAGE_BYTES);
@@ -296,8 +277,8 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   int k = 0;
   bool ok = true;
   for (; k < n_my; ++k) {
-    const int st = k % STAGES;
-    const bool landed = mbar_wait(&bars[warp * STAGES + st], (k / STAGES) & 1, &g_status_decode);
+    const int st = (kb + k) % STAGES;
+    const bool landed = mbar_wait(&bars[warp * STAGES + st], ((kb + k) / STAGES) & 1, &g_status_decode);
     if (!__all_sync(0xffffffffu, landed)) {  // leave the loop together
       ok = false;
       break;
@@ -377,14 +358,14 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
   if (!ok) {
     // drain this warp's loads still in flight (bounded) before the ring is reused
     for (int kk = k + 1; kk < n_my && kk < k + STAGES; ++kk) {
-      const int st = kk % STAGES;
-      mbar_wait(&bars[warp * STAGES + st], (kk / STAGES) & 1, &g_status_decode);
+      const int st = (kb + kk) % STAGES;
+      mbar_wait(&bars[warp * STAGES + st], ((kb + kk) / STAGES) & 1, &g_status_decode);
     }
   }
 
   l0 = warp_sum_xor(l0, 4);
   l1 = warp_sum_xor(l1, 4);
-  __syncthreads();  // every warp is done with its ring
+  sync();  // every warp is done with its ring
 
   float* cm = reinterpret_cast<float*>(smem);
   float* cl = cm + NW * 8;
@@ -405,8 +386,143 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_const
     c1[0] = o[mt][2];
     c1[1] = o[mt][3];
   }
+  sync();
+  combine_and_store<__nv_bfloat16, NW>(p, cm, cl, co, part, g, s, orow, tid);
+  kb += n_my;
+  return ok;
+}
+
+template <int D, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV,
+                                                               const DecodeParams p) {
+  using Shape = Bf16DecodeShape<D>;
+  constexpr int STAGE_BYTES = Shape::kStageBytes;
+  static_assert(NW * (64 + D * 32) <= NW * STAGES * STAGE_BYTES, "combine area must fit in the ring");
+  // Launched as a programmatic dependent (e.g. of the paged K/V write): every input
+  // is read after the previous grid in the stream has completed.  Only then may the
+  // next grid launch (the merge, which waits for this grid to finish anyway).
+  pdl_wait();
+  pdl_launch_dependents();
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * STAGES * STAGE_BYTES);
+
+  __shared__ int rank_lens[kMaxRankSeqs];
+  __shared__ int rank_found;
+  const int part = blockIdx.x, g = blockIdx.y;
+  const int s = (p.partition_size == 0 && p.S <= kMaxRankSeqs) ? seq_of_rank(p, blockIdx.z, rank_lens, &rank_found)
+                                                                : (int)blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int orow = decode_row(p, s);
+  if (orow < 0) return;  // not a decode of this mixed batch
+  int t0, t1;
+  if (!decode_range<__nv_bfloat16>(p, part, g, s, orow, t0, t1, threadIdx.x, blockDim.x)) return;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    for (int i = 0; i < NW * STAGES; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
   __syncthreads();
-  combine_and_store<__nv_bfloat16, NW>(p, cm, cl, co, part, g, s, orow);
+  int kb = 0;
+  decode_bf16_item<D, NW, STAGES>(tmK, tmV, p, smem, bars, part, g, s, orow, t0, t1, warp, lane, threadIdx.x, kb,
+                                  [] { __syncthreads(); });
+}
+
+// bf16 decode configuration: warps per CTA and ring depth per warp.
+#ifndef METIS_DECODE_WARPS
+#define METIS_DECODE_WARPS 4
+#endif
+#ifndef METIS_DECODE_STAGES
+#define METIS_DECODE_STAGES 3
+#endif
+constexpr int kBf16Warps = METIS_DECODE_WARPS;
+constexpr int kBf16Stages = METIS_DECODE_STAGES;
+
+// ---------------------------------------------------------------------------
+// the decodes of a mixed chunked-prefill batch, beside the chunk kernel
+// ---------------------------------------------------------------------------
+// The chunk kernel takes whole SMs.  Beside it, the batch's decodes run on the
+// first n_ctas SMs only (the prefill schedule kernel sizes n_ctas from the batch's
+// decode bytes and chunk FLOPs) rather than on every SM for a shorter time.  One
+// CTA per SM (its shared memory request sees to that), kDecGroups groups of
+// kBf16Warps warps each; a group takes (sequence, KV head) items -- sequences
+// longest first -- from a counter that the schedule kernel zeroed.
+constexpr int kDecGroups = 2;
+
+template <int D>
+constexpr int dec_beside_smem_bytes() {
+  constexpr int need = 1024 + kDecGroups * kBf16Warps * kBf16Stages * (Bf16DecodeShape<D>::kStageBytes + 8);
+  return need > 116 * 1024 ? need : 116 * 1024;  // never two CTAs on one SM
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecGroups * kBf16Warps * 32, 1)
+    decode_rows_beside_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                              const DecodeParams p, const int* n_ctas, int* next_item) {
+  constexpr int NW = kBf16Warps, STAGES = kBf16Stages, GT = NW * 32;
+  constexpr int STAGE_BYTES = Bf16DecodeShape<D>::kStageBytes;
+  static_assert(NW * (64 + D * 32) <= NW * STAGES * STAGE_BYTES, "combine area must fit in the ring");
+  pdl_wait();  // the schedule kernel (n_ctas, the zeroed counter) and every kernel before it completed
+  if ((int)blockIdx.x >= __ldcg(n_ctas)) return;
+  pdl_launch_dependents();  // every CTA of the grid has waited by now: the chunk kernel may launch
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
+  __shared__ int rank_seq[kMaxRankSeqs];
+  __shared__ int lens[kMaxRankSeqs];
+  __shared__ int n_dec;
+  __shared__ int item_slot[kDecGroups];
+  // the batch's decodes, longest first (larger batches: in sequence order)
+  const bool ranked = p.S <= kMaxRankSeqs;
+  if (ranked) {
+    if (threadIdx.x == 0) n_dec = 0;
+    for (int i = threadIdx.x; i < p.S; i += blockDim.x)
+      lens[i] = decode_row(p, i) < 0 ? -1 : min(max(p.seq_lens[i], 0), p.cap);
+    __syncthreads();
+    for (int c = threadIdx.x; c < p.S; c += blockDim.x) {
+      const int Lc = lens[c];
+      if (Lc < 0) continue;
+      int r = 0;
+      for (int k = 0; k < p.S; ++k) r += (lens[k] > Lc) || (lens[k] == Lc && k < c);
+      rank_seq[r] = c;
+      atomicAdd(&n_dec, 1);
+    }
+  }
+  const int grp = threadIdx.x / GT, tid = threadIdx.x - grp * GT;
+  const int warp = tid >> 5, lane = tid & 31;
+  uint8_t* gsmem = smem + grp * NW * STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecGroups * NW * STAGES * STAGE_BYTES) + grp * NW * STAGES;
+  if (tid == 0) {
+    if (grp == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    for (int i = 0; i < NW * STAGES; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int n_items = (ranked ? n_dec : p.S) * p.G;
+  auto gsync = [grp] { named_barrier_sync(1 + grp, GT); };
+  int kb = 0;  // this warp's ring position, across the group's items
+  for (;;) {
+    gsync();  // the previous item's combine is done with the ring, and the slot was read
+    if (tid == 0) item_slot[grp] = atomicAdd(next_item, 1);
+    gsync();
+    const int it = item_slot[grp];
+    if (it >= n_items) break;
+    const int rank = it / p.G, g = it - rank * p.G;
+    const int s = ranked ? rank_seq[rank] : rank;
+    const int orow = decode_row(p, s);
+    if (orow < 0) continue;  // not a decode (unranked order only)
+    int t0, t1;
+    if (!decode_range<__nv_bfloat16>(p, 0, g, s, orow, t0, t1, tid, GT)) continue;
+    if (!decode_bf16_item<D, NW, STAGES>(tmK, tmV, p, gsmem, bars, 0, g, s, orow, t0, t1, warp, lane, tid, kb, gsync))
+      break;  // a wait gave up (flagged); the group stops
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -427,7 +543,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
   const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int t0, t1;
-  if (!decode_range<float>(p, part, g, s, s, t0, t1)) return;
+  if (!decode_range<float>(p, part, g, s, s, t0, t1, threadIdx.x, blockDim.x)) return;
 
   const float* q = reinterpret_cast<const float*>(p.q) + ((size_t)s * p.H + (size_t)g * p.r) * D;
   float qv[8][DPL];
@@ -505,7 +621,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) decode_f32_kernel(const float*
 #pragma unroll
     for (int i = 0; i < DPL; ++i) co[((size_t)warp * D + lane * DPL + i) * 8 + h] = o[h][i];
   __syncthreads();
-  combine_and_store<float, kF32Warps>(p, cm, cl, co, part, g, s, s);
+  combine_and_store<float, kF32Warps>(p, cm, cl, co, part, g, s, s, threadIdx.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -767,27 +883,24 @@ static int effective_max_len(int max_seq_len, int max_blocks, int block_size) {
   return (int)std::min<long long>((long long)max_blocks * block_size, (long long)max_seq_len);
 }
 
-// bf16 decode configuration: warps per CTA and ring depth per warp.
-#ifndef METIS_DECODE_WARPS
-#define METIS_DECODE_WARPS 4
-#endif
-#ifndef METIS_DECODE_STAGES
-#define METIS_DECODE_STAGES 3
-#endif
-constexpr int kBf16Warps = METIS_DECODE_WARPS;
-constexpr int kBf16Stages = METIS_DECODE_STAGES;
+// TMA maps of the K and V caches: 16-token x 64-dim boxes of one KV head.
+template <int D>
+static int encode_kv_maps(const DecodeParams& p, const void* k_cache, const void* v_cache, CUtensorMap* tmK,
+                          CUtensorMap* tmV) {
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.G, (uint64_t)p.num_blocks * p.bs};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.G * D * 2};
+  const uint32_t box[3] = {64, 1, (uint32_t)kUnit};
+  int rc = encode_tiled(tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_cache, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  return encode_tiled(tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v_cache, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
 template <int D>
 static int launch_bf16(const DecodeParams& p, const void* k_cache, const void* v_cache, dim3 grid, cudaStream_t st) {
   CUtensorMap tmK, tmV;
-  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.G, (uint64_t)p.num_blocks * p.bs};
-  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.G * D * 2};
-  const uint32_t box[3] = {64, 1, (uint32_t)kUnit};
-  int rc = encode_tiled(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_cache, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc) return rc;
-  rc = encode_tiled(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v_cache, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = encode_kv_maps<D>(p, k_cache, v_cache, &tmK, &tmV);
   if (rc) return rc;
   constexpr int smem = bf16_decode_smem_bytes<D, kBf16Warps, kBf16Stages>();
   static int done = 0;
@@ -798,12 +911,9 @@ static int launch_bf16(const DecodeParams& p, const void* k_cache, const void* v
                           p);
 }
 
-// The single-token sequences of a chunked-prefill batch, through the decode
-// kernel (unsplit, longest first): rows = the batch's cu_q_lens.  The caller has
-// validated the shapes (bf16, head_dim 64 or 128, head ratio 1, 2, 4 or 8).
-int launch_decode_rows(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H, int G,
-                       int D, int bs, int max_blocks, int num_blocks, float scale, int cap, cudaStream_t st) {
+static DecodeParams rows_params(const void* q, const int32_t* block_table, const int32_t* seq_lens,
+                                const int32_t* rows, void* out, float* lse_out, int S, int H, int G, int D, int bs,
+                                int max_blocks, int num_blocks, float scale, int cap) {
   DecodeParams p;
   p.q = q;
   p.block_table = block_table;
@@ -825,8 +935,44 @@ int launch_decode_rows(const void* q, const void* k_cache, const void* v_cache, 
   p.max_parts = 1;
   p.cap = cap;
   p.rows = rows;
+  return p;
+}
+
+// The single-token sequences of a chunked-prefill batch, through the decode
+// kernel (unsplit, longest first): rows = the batch's cu_q_lens.  The caller has
+// validated the shapes (bf16, head_dim 64 or 128, head ratio 1, 2, 4 or 8).
+int launch_decode_rows(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H, int G,
+                       int D, int bs, int max_blocks, int num_blocks, float scale, int cap, cudaStream_t st) {
+  const DecodeParams p =
+      rows_params(q, block_table, seq_lens, rows, out, lse_out, S, H, G, D, bs, max_blocks, num_blocks, scale, cap);
   const dim3 grid(1u, (unsigned)G, (unsigned)S);
   return D == 64 ? launch_bf16<64>(p, k_cache, v_cache, grid, st) : launch_bf16<128>(p, k_cache, v_cache, grid, st);
+}
+
+template <int D>
+static int launch_beside(const DecodeParams& p, const void* k_cache, const void* v_cache, const int* n_ctas,
+                         int* next_item, int grid, cudaStream_t st) {
+  CUtensorMap tmK, tmV;
+  int rc = encode_kv_maps<D>(p, k_cache, v_cache, &tmK, &tmV);
+  if (rc) return rc;
+  constexpr int smem = dec_beside_smem_bytes<D>();
+  static int done = 0;
+  auto kern = decode_rows_beside_kernel<D>;
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem, &done);
+  if (rc) return rc;
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(kDecGroups * kBf16Warps * 32), (size_t)smem, st,
+                          "decode_rows_beside_kernel launch", tmK, tmV, p, n_ctas, next_item);
+}
+
+int launch_decode_rows_beside(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H,
+                              int G, int D, int bs, int max_blocks, int num_blocks, float scale, int cap,
+                              const int* n_ctas, int* next_item, int grid, cudaStream_t st) {
+  const DecodeParams p =
+      rows_params(q, block_table, seq_lens, rows, out, lse_out, S, H, G, D, bs, max_blocks, num_blocks, scale, cap);
+  return D == 64 ? launch_beside<64>(p, k_cache, v_cache, n_ctas, next_item, grid, st)
+                 : launch_beside<128>(p, k_cache, v_cache, n_ctas, next_item, grid, st);
 }
 
 }  // namespace metis

@@ -65,6 +65,16 @@ int launch_decode_rows(const void* q, const void* k_cache, const void* v_cache, 
                        const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H, int G,
                        int D, int bs, int max_blocks, int num_blocks, float scale, int cap, cudaStream_t st);
 
+// The same, persistent, beside the chunk kernel: one CTA per SM in a grid of `grid`
+// CTAs, of which the first *n_ctas (device value, written by the prefill schedule
+// kernel before this grid reads it) take (sequence, KV head) items from the
+// counter *next_item (zeroed by that kernel); the others exit at once.  Every CTA
+// lets the next grid launch only after waiting for the previous one.
+int launch_decode_rows_beside(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, const int32_t* rows, void* out, float* lse_out, int S, int H,
+                              int G, int D, int bs, int max_blocks, int num_blocks, float scale, int cap,
+                              const int* n_ctas, int* next_item, int grid, cudaStream_t st);
+
 // Per-translation-unit device status words.
 int decode_status(uint32_t* bits, int clear);
 int prefill_status(uint32_t* bits, int clear);

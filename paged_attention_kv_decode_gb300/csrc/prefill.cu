@@ -98,6 +98,15 @@ struct PrefillParams {
   int S, T, H, G, r, Tq, bs, max_blocks, num_blocks, cap;
   float scale_log2;
   int skip_decodes;  // single-token sequences are served by the decode kernel: list no tiles for them
+  // Decodes beside the chunk kernel (dec_ctas != NULL): the schedule kernel writes the
+  // number of SMs the decode kernel keeps (*dec_ctas) and zeroes its item counter
+  // (*dec_next); this kernel then launches behind that decode kernel, which lets it
+  // launch only once its CTAs have waited for the schedule, so the list is ready at
+  // launch: no wait at the start, the wait for the decode grid just before exiting.
+  int* dec_ctas;
+  int* dec_next;
+  int num_sms, D;
+  int wait_at_exit;
 };
 
 // Shared-memory layout (all tiles 128-byte swizzled, [64-column half][row][128 B]).
@@ -161,6 +170,14 @@ __device__ __forceinline__ int pf_kv_tiles(int L, int q_len, int tile, int Tq) {
 // schedule: the (sequence, query-tile pair) work list, heaviest first
 // ---------------------------------------------------------------------------
 constexpr int kSchedThreads = 1024;
+// One SM's rates, for sizing the decodes' share of SMs beside the chunks: decode
+// K/V bytes per second while the chunks run (a CTA of two 4-warp groups, each warp
+// a 3-stage ring: ~192 KB in flight, which the loaded memory system turns into
+// ~65 GB/s; measured on a GB300 as the setting that balances the mixed batch of 16
+// chunks and 48 decodes, with fewer decode SMs far worse than more), and the chunk
+// kernel's FLOP/s (the chunks alone reach ~1.07 PFLOP/s on 152 SMs).
+constexpr double kDecSmBytesPerS = 65e9;
+constexpr double kChunkSmFlopsPerS = 7.0e12;
 
 __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const PrefillParams p, int4* items,
                                                                           int* count, int max_items) {
@@ -173,11 +190,17 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
   const int pair_tokens = 2 * p.Tq;
   int local = 0;
+  double dec_tok = 0.0, chunk_qk = 0.0;  // decode tokens read; (query, key) pairs of the chunks
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
     const bool routed = p.skip_decodes && p.cu_q_lens[s + 1] - p.cu_q_lens[s] == 1;
     pf_lengths(p, s, L, q_len, routed);  // a routed decode's content errors are flagged here
-    if (!routed) local += (q_len + pair_tokens - 1) / pair_tokens;
+    if (!routed) {
+      local += (q_len + pair_tokens - 1) / pair_tokens;
+      chunk_qk += (double)q_len * (L - q_len) + 0.5 * (double)q_len * (q_len + 1);
+    } else {
+      dec_tok += L;
+    }
   }
   int all;
   int pos = block_exclusive_scan<kSchedThreads>(local, warp_sums, &all);
@@ -210,6 +233,34 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
       items[rank] = me;
     }
   }
+  if (p.dec_ctas) {
+    // SMs for the decodes beside the chunks: decodes on k SMs and chunks on the
+    // other N - k finish together when k / N = d / (d + c), with d and c the SM time
+    // each kind needs alone (rates of one SM: kDecSmBytesPerS, kChunkSmFlopsPerS)
+    __shared__ double red[2][kSchedThreads / 32];
+    for (int o = 16; o > 0; o >>= 1) {
+      dec_tok += __shfl_xor_sync(0xffffffffu, dec_tok, o);
+      chunk_qk += __shfl_xor_sync(0xffffffffu, chunk_qk, o);
+    }
+    if ((tid & 31) == 0) {
+      red[0][tid >> 5] = dec_tok;
+      red[1][tid >> 5] = chunk_qk;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      double d = 0.0, c = 0.0;
+      for (int w = 0; w < kSchedThreads / 32; ++w) {
+        d += red[0][w];
+        c += red[1][w];
+      }
+      d *= (double)p.G * p.D * 4.0 / kDecSmBytesPerS;   // K and V rows of every decode, bf16
+      c *= (double)p.H * p.D * 4.0 / kChunkSmFlopsPerS;  // QK^T and PV of every chunk query
+      int k = 0;
+      if (d > 0.0) k = c > 0.0 ? (int)ceil(p.num_sms * d / (d + c)) : p.num_sms;
+      *p.dec_ctas = min(max(k, d > 0.0 ? 1 : 0), p.num_sms);
+      *p.dec_next = 0;
+    }
+  }
   if (tid == 0) {
     *count = total;
     *p.unit_head = 0;
@@ -228,7 +279,7 @@ struct PfUnit {
 __device__ __forceinline__ bool pf_unit(const PrefillParams& p, int u, bool flag, PfUnit& it) {
   const int item_idx = u / p.G;
   it.g = u - item_idx * p.G;
-  const int4 v = p.items[item_idx];
+  const int4 v = __ldcg(p.items + item_idx);  // written by this call's schedule kernel: read from L2
   it.s = v.x;
   it.pair = v.y;
   pf_lengths(p, it.s, it.L, it.q_len, flag && it.g == 0);
@@ -247,7 +298,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
                                                                        const PrefillParams p) {
   using Sh = PfShape<D>;
   constexpr int HALVES = Sh::kHalves;
-  pdl_wait();  // the schedule kernel's items are complete and visible
+  if (!p.wait_at_exit) pdl_wait();  // the schedule kernel's items are complete and visible
   extern __shared__ uint8_t smem_raw[];
   const uint32_t slack = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + slack;
@@ -272,8 +323,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   volatile int* unit_slot = reinterpret_cast<volatile int*>(bars + PfBar::kCount + 2);  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int units = *p.item_count * p.G;
-  if ((int)blockIdx.x >= units) return;
+  const int units = __ldcg(p.item_count) * p.G;
+  if ((int)blockIdx.x >= units) {
+    if (p.wait_at_exit) pdl_wait();  // complete only after the decode grid in front of this one
+    return;
+  }
 
   if (threadIdx.x == 0) {
     // full barriers: one arrival per producer warp of the ring; p_full: 128 softmax threads
@@ -686,6 +740,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (p.wait_at_exit) pdl_wait();  // complete only after the decode grid in front of this one
 }
 
 // ---------------------------------------------------------------------------
@@ -709,15 +764,24 @@ static size_t prefill_max_items(int num_seqs, int num_tokens, int Tq) {
   return (size_t)(num_tokens + 2 * Tq - 1) / (2 * Tq) + (size_t)num_seqs;
 }
 
-template <int D>
+// The schedule kernel, then `between(p)` (the decodes of a mixed batch, or
+// nothing), then the chunk kernel.
+template <int D, typename Between>
 static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_cache, const void* v_cache,
-                          void* workspace, size_t max_items, cudaStream_t st) {
+                          void* workspace, size_t max_items, int sms, cudaStream_t st, Between between) {
   PrefillParams p = p0;
   int* count = reinterpret_cast<int*>(workspace);
   int4* items = reinterpret_cast<int4*>(reinterpret_cast<char*>(workspace) + 256);
   p.items = items;
   p.item_count = count;
   p.unit_head = count + 1;
+  if (p.skip_decodes) {
+    p.dec_ctas = count + 2;
+    p.dec_next = count + 3;
+    p.wait_at_exit = 1;
+  }
+  p.num_sms = sms;
+  p.D = D;
   CUtensorMap tmQ, tmK, tmV;
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)p.H, (uint64_t)p.T};
   const uint64_t qstr[2] = {(uint64_t)D * 2, (uint64_t)p.H * D * 2};
@@ -731,10 +795,12 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
   if (rc) return rc;
   rc = encode_tiled(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v_cache, kdims, kstr, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  // a programmatic dependent of the kernel before it (the paged K/V write, or the
-  // decodes of this batch): its launch overlaps that kernel's tail
+  // a programmatic dependent of the kernel before it (e.g. the paged K/V write): its
+  // launch overlaps that kernel's tail
   rc = launch_dependent(prefill_schedule_kernel, dim3(1), dim3(kSchedThreads), 0, st, "prefill_schedule_kernel launch",
                         p, items, count, (int)max_items);
+  if (rc) return rc;
+  rc = between(p);
   if (rc) return rc;
   constexpr int smem = PfShape<D>::kSmem;
   static int done = 0;
@@ -754,10 +820,7 @@ static int launch_prefill(const PrefillParams& p0, const void* q, const void* k_
     regs_checked = 1;
   }
   // persistent: at most one CTA per SM, each taking units from the list as it goes
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return fail(METIS_E_CUDA, "querying the SM count: %s", cudaGetErrorString(e));
+  // (beside the decodes: the CTAs past the SMs they keep start as their CTAs finish)
   const size_t grid = std::min<size_t>(max_items * p.G, (size_t)std::max(sms, 1));
   return launch_dependent(kern, dim3((unsigned)grid), dim3(kPfThreads), smem, st, "prefill_bf16_kernel launch", tmQ,
                           tmK, tmV, p);
@@ -829,15 +892,24 @@ extern "C" int metis_paged_attn_prefill_chunk(const void* q, const int32_t* cu_q
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // Single-token sequences (the decodes of a mixed batch) go through the decode
   // kernel, which streams their K/V at the memory rate (a 128-row query tile would
-  // hold r valid rows of them).  It runs first, as an ordinary launch; the schedule
-  // and the chunk kernel follow it.  Head ratios above 8 stay on the chunk path.
+  // hold r valid rows of them).  It runs beside the chunk kernel: the schedule
+  // kernel gives it a share of the SMs in proportion to the decodes' bytes against
+  // the chunks' FLOPs, its other CTAs exit at once, and the chunk kernel -- launched
+  // behind it, which it allows only after its CTAs waited for the schedule -- takes
+  // the remaining SMs at once and the decodes' SMs as they finish.  Head ratios
+  // above 8 stay on the chunk path.
   p.skip_decodes = r <= 8 && num_seqs <= 65535;
-  if (p.skip_decodes) {
-    const int rc = launch_decode_rows(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse_out, num_seqs,
-                                      num_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale,
-                                      p.cap, st);
-    if (rc) return rc;
-  }
-  return head_dim == 128 ? launch_prefill<128>(p, q, k_cache, v_cache, workspace, max_items, st)
-                         : launch_prefill<64>(p, q, k_cache, v_cache, workspace, max_items, st);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(METIS_E_CUDA, "querying the SM count: %s", cudaGetErrorString(e));
+  sms = std::max(sms, 1);
+  auto between = [&](const PrefillParams& pp) -> int {
+    if (!pp.skip_decodes) return METIS_OK;
+    return launch_decode_rows_beside(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse_out, num_seqs,
+                                     num_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale,
+                                     pp.cap, pp.dec_ctas, pp.dec_next, sms, st);
+  };
+  return head_dim == 128 ? launch_prefill<128>(p, q, k_cache, v_cache, workspace, max_items, sms, st, between)
+                         : launch_prefill<64>(p, q, k_cache, v_cache, workspace, max_items, sms, st, between);
 }
