@@ -152,6 +152,30 @@ def test_bad_block_id_and_q_len_are_flagged():
     assert pa.metis_read_status() & pa.STATUS_BAD_Q_LEN
 
 
+@pytest.mark.parametrize("D,bs,H,G", [(64, 32, 16, 8), (128, 16, 32, 8)])
+def test_decodes_beside_chunks(D, bs, H, G):
+    """Decodes and chunks in one batch: the decodes run on their share of the SMs beside
+    the chunk kernel (both kinds must match the oracle, lse included)."""
+    prefixes = [900, 0, 2000, 5, 300, 1500, 64, 3000, 17, 700] * 3
+    q_lens = [1, 256, 1, 1, 128, 1, 200, 1, 1, 64] * 3
+    case = wl.make_prefill_case(71 + D, prefixes, q_lens, H=H, G=G, D=D, bs=bs, dtype=torch.bfloat16,
+                                extra_blocks=2, poison=True)
+    check(case)
+
+
+def test_bad_block_id_in_a_decode():
+    """A decode with a block id outside the pool, beside chunks: flagged, finite, the rest exact."""
+    case = wl.make_prefill_case(73, [200, 100, 50], [1, 64, 1], H=8, G=2, D=128, bs=16, dtype=torch.bfloat16)
+    bt = case.block_table.clone()
+    bt[0, 3] = case.num_blocks + 5
+    out, _ = gpu_prefill(case, block_table=bt)
+    assert pa.metis_read_status() & pa.STATUS_BAD_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ref_o, _ = oracle_prefill(case)
+    cu = case.cu_q_lens.numpy()
+    assert_parity(out[cu[1]:], ref_o[cu[1]:], torch.bfloat16)
+
+
 def test_empty_chunks_and_more_units_than_ctas():
     """Chunks of 0 tokens (nothing to compute: the unit fetcher skips them) between real
     ones, and more (item, KV head) units than SMs, taken from the list as the CTAs free up."""
