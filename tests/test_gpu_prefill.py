@@ -152,7 +152,7 @@ def test_bad_block_id_and_q_len_are_flagged():
     assert pa.metis_read_status() & pa.STATUS_BAD_Q_LEN
 
 
-@pytest.mark.parametrize("D,bs,H,G", [(64, 32, 16, 8), (128, 16, 32, 8)])
+@pytest.mark.parametrize("D,bs,H,G", [(64, 32, 16, 8), (128, 16, 32, 8), (64, 16, 8, 1), (128, 64, 16, 16)])
 def test_decodes_beside_chunks(D, bs, H, G):
     """Decodes and chunks in one batch: the decodes run on their share of the SMs beside
     the chunk kernel (both kinds must match the oracle, lse included)."""
