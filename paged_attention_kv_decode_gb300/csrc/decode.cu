@@ -476,6 +476,7 @@ __global__ void __launch_bounds__(kDecGroups * kBf16Warps * 32, 1)
   __shared__ int lens[kMaxRankSeqs];
   __shared__ int n_dec;
   __shared__ int item_slot[kDecGroups];
+  __shared__ int gave_up[kDecGroups];  // a warp of the group gave up a wait: the group stops
   // the batch's decodes, longest first (larger batches: in sequence order)
   const bool ranked = p.S <= kMaxRankSeqs;
   if (ranked) {
@@ -503,6 +504,7 @@ __global__ void __launch_bounds__(kDecGroups * kBf16Warps * 32, 1)
     }
     for (int i = 0; i < NW * STAGES; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
+    gave_up[grp] = 0;
   }
   __syncthreads();
   const int n_items = (ranked ? n_dec : p.S) * p.G;
@@ -510,6 +512,7 @@ __global__ void __launch_bounds__(kDecGroups * kBf16Warps * 32, 1)
   int kb = 0;  // this warp's ring position, across the group's items
   for (;;) {
     gsync();  // the previous item's combine is done with the ring, and the slot was read
+    if (gave_up[grp]) break;  // read after the barrier: the whole group leaves together
     if (tid == 0) item_slot[grp] = atomicAdd(next_item, 1);
     gsync();
     const int it = item_slot[grp];
@@ -520,8 +523,11 @@ __global__ void __launch_bounds__(kDecGroups * kBf16Warps * 32, 1)
     if (orow < 0) continue;  // not a decode (unranked order only)
     int t0, t1;
     if (!decode_range<__nv_bfloat16>(p, 0, g, s, orow, t0, t1, tid, GT)) continue;
-    if (!decode_bf16_item<D, NW, STAGES>(tmK, tmV, p, gsmem, bars, 0, g, s, orow, t0, t1, warp, lane, tid, kb, gsync))
-      break;  // a wait gave up (flagged); the group stops
+    // A wait that gave up (flagged) is seen by its warp only: every warp of the group
+    // still reaches the item's barriers and the next one above, where they all stop.
+    if (!decode_bf16_item<D, NW, STAGES>(tmK, tmV, p, gsmem, bars, 0, g, s, orow, t0, t1, warp, lane, tid, kb, gsync) &&
+        lane == 0)
+      gave_up[grp] = 1;
   }
 }
 
