@@ -43,8 +43,9 @@
 // Persistent mixed batch: a small schedule kernel lists the (sequence,
 // query-tile pair) items heaviest first -- the chunks of every length in one
 // list -- and one CTA per SM takes units (item, KV head) from that list as it
-// goes (warp 14 claims the next one with an atomic and publishes it to the other
-// warps through a two-slot ring).  Every role keeps its ring and barrier counters
+// goes (warp 14 claims the next one with an atomic once every warp has taken the
+// current one, and publishes it with its derived fields to the other warps through
+// a two-slot ring).  Every role keeps its ring and barrier counters
 // running across units, so the next unit's queries (warp 13, once the current
 // unit's last QK has completed) and K/V tiles stream in while the current unit's
 // last softmax, PV and epilogue drain.
@@ -172,12 +173,12 @@ __device__ __forceinline__ int pf_kv_tiles(int L, int q_len, int tile, int Tq) {
 constexpr int kSchedThreads = 1024;
 // One SM's rates, for sizing the decodes' share of SMs beside the chunks: decode
 // K/V bytes per second while the chunks run (a CTA of two 4-warp groups, each warp
-// a 3-stage ring: ~192 KB in flight, which the loaded memory system turns into
-// ~65 GB/s; measured on a GB300 as the setting that balances the mixed batch of 16
-// chunks and 48 decodes, with fewer decode SMs far worse than more), and the chunk
-// kernel's FLOP/s (the chunks alone reach ~1.07 PFLOP/s on 152 SMs).
-constexpr double kDecSmBytesPerS = 65e9;
-constexpr double kChunkSmFlopsPerS = 7.0e12;
+// a 3-stage ring: ~192 KB in flight; timestamps on a GB300 show 453 MB of decodes
+// taking ~253 us on 24 SMs beside 16 chunks of 512, i.e. ~75 GB/s per SM.  Too few
+// decode SMs, so that the decodes finish last, costs far more than a few too many),
+// and the chunk kernel's FLOP/s (the chunks alone reach ~1.07 PFLOP/s on 152 SMs).
+constexpr float kDecSmBytesPerS = 75e9f;
+constexpr float kChunkSmFlopsPerS = 7.0e12f;
 
 __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const PrefillParams p, int4* items,
                                                                           int* count, int max_items) {
@@ -190,26 +191,72 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
   const int s0 = min(p.S, tid * per), s1 = min(p.S, s0 + per);
   const int pair_tokens = 2 * p.Tq;
   int local = 0;
-  double dec_tok = 0.0, chunk_qk = 0.0;  // decode tokens read; (query, key) pairs of the chunks
+  // decode tokens read; (query, key) pairs of the chunks.  Integers and a float ratio:
+  // this GPU's fp64 rate is a small fraction of its fp32 rate.
+  long long dec_tok = 0, chunk_qk = 0;
+  int L_first = 0, q_first = 0;  // this thread's first sequence, kept for the listing pass
+  bool routed_first = false;
   for (int s = s0; s < s1; ++s) {
     int L, q_len;
     const bool routed = p.skip_decodes && p.cu_q_lens[s + 1] - p.cu_q_lens[s] == 1;
     pf_lengths(p, s, L, q_len, routed);  // a routed decode's content errors are flagged here
+    if (s == s0) {
+      L_first = L;
+      q_first = q_len;
+      routed_first = routed;
+    }
     if (!routed) {
       local += (q_len + pair_tokens - 1) / pair_tokens;
-      chunk_qk += (double)q_len * (L - q_len) + 0.5 * (double)q_len * (q_len + 1);
+      chunk_qk += (long long)q_len * (L - q_len) + (long long)q_len * (q_len + 1) / 2;
     } else {
       dec_tok += L;
     }
   }
+  // The decodes' share of SMs, from warp sums published before the scan's barriers
+  // and combined by the last warp (no sequences there unless S > 992): off the path
+  // of the listing and the sort.
+  __shared__ long long red[2][kSchedThreads / 32];
+  static_assert(kSchedThreads == 32 * 32, "one warp combines the warp sums");
+  const int lane = tid & 31, warp = tid >> 5;
+  if (p.dec_ctas) {
+    for (int o = 16; o > 0; o >>= 1) {
+      dec_tok += __shfl_xor_sync(0xffffffffu, dec_tok, o);
+      chunk_qk += __shfl_xor_sync(0xffffffffu, chunk_qk, o);
+    }
+    if (lane == 0) {
+      red[0][warp] = dec_tok;
+      red[1][warp] = chunk_qk;
+    }
+  }
   int all;
   int pos = block_exclusive_scan<kSchedThreads>(local, warp_sums, &all);
+  if (p.dec_ctas && warp == kSchedThreads / 32 - 1) {
+    // SMs for the decodes beside the chunks: decodes on k SMs and chunks on the
+    // other N - k finish together when k / N = d / (d + c), with d and c the SM time
+    // each kind needs alone (rates of one SM: kDecSmBytesPerS, kChunkSmFlopsPerS)
+    long long dt = red[0][lane], cq = red[1][lane];
+    for (int o = 16; o > 0; o >>= 1) {
+      dt += __shfl_xor_sync(0xffffffffu, dt, o);
+      cq += __shfl_xor_sync(0xffffffffu, cq, o);
+    }
+    if (lane == 0) {
+      const float d = (float)dt * ((float)p.G * p.D * 4.0f / kDecSmBytesPerS);   // K and V rows of every decode
+      const float c = (float)cq * ((float)p.H * p.D * 4.0f / kChunkSmFlopsPerS);  // QK^T and PV of every chunk query
+      int k = 0;
+      if (dt > 0) k = cq > 0 ? (int)ceilf(p.num_sms * (d / (d + c))) : p.num_sms;
+      *p.dec_ctas = min(max(k, dt > 0 ? 1 : 0), p.num_sms);
+      *p.dec_next = 0;
+    }
+  }
   const int total = min(all, max_items);
   const bool sort = total <= kSortMax;
   for (int s = s0; s < s1; ++s) {
-    int L, q_len;
-    pf_lengths(p, s, L, q_len, false);
-    const bool routed = p.skip_decodes && p.cu_q_lens[s + 1] - p.cu_q_lens[s] == 1;
+    int L = L_first, q_len = q_first;
+    bool routed = routed_first;
+    if (s != s0) {
+      pf_lengths(p, s, L, q_len, false);
+      routed = p.skip_decodes && p.cu_q_lens[s + 1] - p.cu_q_lens[s] == 1;
+    }
     const int np = routed ? 0 : (q_len + pair_tokens - 1) / pair_tokens;
     for (int t = 0; t < np; ++t, ++pos) {
       if (pos >= total) break;
@@ -222,43 +269,26 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
     }
   }
   if (sort) {
+    // rank = number of items heavier than this one (ties: earlier in the list first);
+    // `ways` threads (a power of two, within a warp) count a share of the list each
     __syncthreads();
-    for (int i = tid; i < total; i += kSchedThreads) {
-      const int4 me = buf[i];
+    int ways = 1;
+    while (ways < 32 && total * ways * 2 <= kSchedThreads) ways *= 2;
+    const int sub = tid & (ways - 1);
+    for (int base = 0; base < total; base += kSchedThreads / ways) {  // the same trip count in every thread
+      const int i = base + tid / ways;
+      const bool live = i < total;
+      int4 me = make_int4(0, 0, 0, 0);
       int rank = 0;
-      for (int k = 0; k < total; ++k) {
-        const int w = buf[k].z;
-        rank += (w > me.z) || (w == me.z && k < i);
+      if (live) {
+        me = buf[i];
+        for (int k = sub; k < total; k += ways) {
+          const int w = buf[k].z;
+          rank += (w > me.z) || (w == me.z && k < i);
+        }
       }
-      items[rank] = me;
-    }
-  }
-  if (p.dec_ctas) {
-    // SMs for the decodes beside the chunks: decodes on k SMs and chunks on the
-    // other N - k finish together when k / N = d / (d + c), with d and c the SM time
-    // each kind needs alone (rates of one SM: kDecSmBytesPerS, kChunkSmFlopsPerS)
-    __shared__ double red[2][kSchedThreads / 32];
-    for (int o = 16; o > 0; o >>= 1) {
-      dec_tok += __shfl_xor_sync(0xffffffffu, dec_tok, o);
-      chunk_qk += __shfl_xor_sync(0xffffffffu, chunk_qk, o);
-    }
-    if ((tid & 31) == 0) {
-      red[0][tid >> 5] = dec_tok;
-      red[1][tid >> 5] = chunk_qk;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      double d = 0.0, c = 0.0;
-      for (int w = 0; w < kSchedThreads / 32; ++w) {
-        d += red[0][w];
-        c += red[1][w];
-      }
-      d *= (double)p.G * p.D * 4.0 / kDecSmBytesPerS;   // K and V rows of every decode, bf16
-      c *= (double)p.H * p.D * 4.0 / kChunkSmFlopsPerS;  // QK^T and PV of every chunk query
-      int k = 0;
-      if (d > 0.0) k = c > 0.0 ? (int)ceil(p.num_sms * d / (d + c)) : p.num_sms;
-      *p.dec_ctas = min(max(k, d > 0.0 ? 1 : 0), p.num_sms);
-      *p.dec_next = 0;
+      for (int o = ways >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+      if (live && sub == 0) items[rank] = me;
     }
   }
   if (tid == 0) {
@@ -321,6 +351,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PfBar::kCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + PfBar::kCount + 1);
   volatile int* unit_slot = reinterpret_cast<volatile int*>(bars + PfBar::kCount + 2);  // [2]
+  __shared__ PfUnit unit_info[2];  // the published unit, derived once by the fetcher
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = __ldcg(p.item_count) * p.G;
@@ -362,16 +393,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   // every role calls waits with all 32 lanes: agree on the outcome before any warp-collective op
   auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(bar, parity)); };
   // The k-th unit of this CTA, from the unit ring: 1 = a unit, 0 = no more, -1 = aborted.
-  auto next_unit = [&](uint32_t& k, PfUnit& it, bool flag) -> int {
+  // The fetcher publishes the unit's derived fields with it, so that no role waits on
+  // global loads at a unit boundary.
+  auto next_unit = [&](uint32_t& k, PfUnit& it) -> int {
     const int slot = k & 1;
     if (!wait_all(&unit_full[slot], (k >> 1) & 1)) return -1;
     const int u = unit_slot[slot];
+    if (u >= 0) it = unit_info[slot];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&unit_empty[slot]);
+    if (lane == 0) mbar_arrive(&unit_empty[slot]);  // release: the reads above are done
     ++k;
-    if (u < 0) return 0;
-    pf_unit(p, u, flag, it);
-    return 1;
+    return u < 0 ? 0 : 1;
   };
 
   // Ring positions run on across units: K/V tile t (counted over every unit this
@@ -395,7 +427,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     uint32_t t = 0, k = 0;                     // tiles issued so far, units read
     bool ok = true;
     PfUnit it;
-    while (ok && next_unit(k, it, false) > 0) {
+    while (ok && next_unit(k, it) > 0) {
       const int32_t* bt_row = p.block_table + (size_t)it.s * p.max_blocks;
       for (int j = 0; j < it.n_kv; ++j, ++t) {
         const int st = t % depth;
@@ -460,7 +492,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     bool ok = true;
     PfUnit it;
     while (ok) {
-      const int r = next_unit(k, it, false);
+      const int r = next_unit(k, it);
       if (r <= 0) {
         ok = r == 0;
         break;
@@ -549,7 +581,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     if (lane == 0) tma_prefetch_desc(&tmQ);
     uint32_t n_units = 0, k = 0;
     PfUnit it;
-    while (next_unit(k, it, false) > 0) {
+    while (next_unit(k, it) > 0) {
       // the previous unit's query tiles stay until its last QK has completed
       if (n_units > 0 && !wait_all(q_free, (n_units - 1) & 1)) break;
       if (lane == 0) {
@@ -571,24 +603,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
   } else if (warp == kMmaWarp + 2) {
     // ------------------------------------------------------------ unit fetcher
     // claims units from the global list, heaviest first, and publishes them to
-    // the other warps through the two-slot unit ring; -1 ends the walk
+    // the other warps through the two-slot unit ring; -1 ends the walk.  Unit k is
+    // claimed only once every warp has taken unit k - 1: one unit of lookahead, so
+    // that at the end of the list no CTA holds small units that an idle CTA could run.
     regs_dec<kRegsMma>();
     uint32_t k = 0;
     for (;;) {
+      const int slot = k & 1;
+      if (k >= 1 && !wait_all(&unit_empty[(k - 1) & 1], ((k - 1) >> 1) & 1)) break;
       int u = 0;
       if (lane == 0) u = atomicAdd(p.unit_head, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
+      PfUnit it;
       if (u < units) {
-        PfUnit it;
         if (!pf_unit(p, u, lane == 0, it)) continue;   // nothing to compute (length errors flagged here)
       } else {
         u = -1;
       }
-      const int slot = k & 1;
-      if (k >= 2 && !wait_all(&unit_empty[slot], ((k >> 1) - 1) & 1)) break;
       if (lane == 0) {
+        if (u >= 0) unit_info[slot] = it;
         unit_slot[slot] = u;
-        mbar_arrive(&unit_full[slot]);
+        mbar_arrive(&unit_full[slot]);  // release: the unit's fields are visible to every waiter
       }
       __syncwarp();
       ++k;
@@ -612,7 +647,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_bf16_kernel(const __gri
     uint32_t ns = 0, npv = 0, k = 0;            // s_full phases consumed, PVs of this group, units read
     bool ok = true;
     PfUnit it;
-    while (ok && next_unit(k, it, false) > 0) {
+    while (ok && next_unit(k, it) > 0) {
       const int nkv = w ? it.n1 : it.n0;
       if (nkv == 0) continue;                   // no second query tile in this unit
       const int L = it.L, q_len = it.q_len;
