@@ -754,23 +754,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const float* __
   if (threadIdx.x == 0 && lse_out) lse_out[sh] = empty ? -INFINITY : M + log2f(W) * kLn2;
 }
 
-// One warp per (sequence, head) when there are few partitions: lanes share the
-// lse reductions and own float4 columns lane, lane + 32, ...
+// The merge of row sh = (sequence, head) over its n partitions by one warp: lanes
+// share the lse reductions and own float4 columns lane, lane + 32, ...
 template <typename OutT>
-__global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* __restrict__ part_out,
-                                                                   const float* __restrict__ part_lse,
-                                                                   const int32_t* __restrict__ seq_lens, int P,
-                                                                   OutT* __restrict__ out,
-                                                                   float* __restrict__ lse_out, int S, int H, int D,
-                                                                   int max_parts, int skip_single) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();  // the partials of the kernel before this one are complete and visible
-  const size_t sh = (size_t)blockIdx.x * (kMergeThreads / 32) + warp;
-  if (sh >= (size_t)S * H) return;
-  const int s = (int)(sh / H);
-  const int L = seq_lens[s];
-  const int n = L > 0 ? min(L / P + (L % P != 0), max_parts) : 0;   // ceil(L / P) without overflow
-  if (skip_single && n <= 1) return;
+__device__ __forceinline__ void merge_row(const float* __restrict__ part_out, const float* __restrict__ part_lse,
+                                          OutT* __restrict__ out, float* __restrict__ lse_out, size_t sh, int n,
+                                          int D, int max_parts, int lane) {
   const float* lrow = part_lse + sh * max_parts;
   float M = -INFINITY;
   for (int i = lane; i < n; i += 32) M = fmaxf(M, lrow[i]);
@@ -827,6 +816,62 @@ __global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* 
   if (lane == 0 && lse_out) lse_out[sh] = empty ? -INFINITY : M + log2f(W) * kLn2;
 }
 
+// One warp per (sequence, head) when there are few partitions.
+template <typename OutT>
+__global__ void __launch_bounds__(kMergeThreads) merge_warp_kernel(const float* __restrict__ part_out,
+                                                                   const float* __restrict__ part_lse,
+                                                                   const int32_t* __restrict__ seq_lens, int P,
+                                                                   OutT* __restrict__ out,
+                                                                   float* __restrict__ lse_out, int S, int H, int D,
+                                                                   int max_parts, int skip_single) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();  // the partials of the kernel before this one are complete and visible
+  const size_t sh = (size_t)blockIdx.x * (kMergeThreads / 32) + warp;
+  if (sh >= (size_t)S * H) return;
+  const int s = (int)(sh / H);
+  const int L = seq_lens[s];
+  const int n = L > 0 ? min(L / P + (L % P != 0), max_parts) : 0;   // ceil(L / P) without overflow
+  if (skip_single && n <= 1) return;
+  merge_row<OutT>(part_out, part_lse, out, lse_out, sh, n, D, max_parts, lane);
+}
+
+// Only the sequences with two or more partitions (the others were written
+// directly), for batches of up to kMergeListThreads sequences: every CTA lists
+// those sequences itself (a scan over seq_lens), and the grid's warps -- one CTA
+// per SM, a single wave -- take their (sequence, head) rows in turn.  Few CTAs
+// instead of one per four rows of every sequence: when most sequences have one
+// partition, most of those CTAs would only check a length and exit.
+constexpr int kMergeListThreads = 512;  // 128 registers a thread: the row merge needs ~94
+template <typename OutT>
+__global__ void __launch_bounds__(kMergeListThreads, 1) merge_split_rows_kernel(
+    const float* __restrict__ part_out, const float* __restrict__ part_lse, const int32_t* __restrict__ seq_lens,
+    int P, OutT* __restrict__ out, float* __restrict__ lse_out, int S, int H, int D, int max_parts) {
+  __shared__ int warp_sums[32];
+  __shared__ int list_s[kMergeListThreads];
+  __shared__ int list_n[kMergeListThreads];
+  pdl_wait();  // the partials of the kernel before this one are complete and visible
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int n = 0;
+  if (tid < S) {
+    const int L = seq_lens[tid];
+    n = L > 0 ? min(L / P + (L % P != 0), max_parts) : 0;
+  }
+  const int split = n >= 2;
+  int total;
+  const int pos = block_exclusive_scan<kMergeListThreads>(split, warp_sums, &total);
+  if (split) {
+    list_s[pos] = tid;
+    list_n[pos] = n;
+  }
+  __syncthreads();
+  const long long rows = (long long)total * H;
+  const long long stride = (long long)gridDim.x * (kMergeListThreads / 32);
+  for (long long r = (long long)blockIdx.x * (kMergeListThreads / 32) + warp; r < rows; r += stride) {
+    const int k = (int)(r / H), h = (int)(r - (long long)k * H);
+    merge_row<OutT>(part_out, part_lse, out, lse_out, (size_t)list_s[k] * H + h, list_n[k], D, max_parts, lane);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -868,6 +913,20 @@ int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t*
                             max_parts, skip_single);
   return launch_dependent(merge_kernel<float>, grid, dim3(kMergeWarps * 32), 0, st, "merge kernel launch", part_out,
                           part_lse, seq_lens, P, reinterpret_cast<float*>(out), lse_out, H, D, max_parts, skip_single);
+}
+
+int launch_merge_split_rows(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,
+                            float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int sms,
+                            cudaStream_t st) {
+  if (S > kMergeListThreads || max_parts > 16 || D > kMergeMaxD)  // outside this kernel's reach
+    return launch_merge_ex(part_out, part_lse, seq_lens, P, out, lse_out, S, H, D, max_parts, out_dtype, 1, st);
+  const dim3 grid((unsigned)std::max(sms, 1));
+  if (out_dtype == METIS_BF16)
+    return launch_dependent(merge_split_rows_kernel<__nv_bfloat16>, grid, dim3(kMergeListThreads), 0, st,
+                            "merge kernel launch", part_out, part_lse, seq_lens, P,
+                            reinterpret_cast<__nv_bfloat16*>(out), lse_out, S, H, D, max_parts);
+  return launch_dependent(merge_split_rows_kernel<float>, grid, dim3(kMergeListThreads), 0, st, "merge kernel launch",
+                          part_out, part_lse, seq_lens, P, reinterpret_cast<float*>(out), lse_out, S, H, D, max_parts);
 }
 
 static int launch_merge(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,

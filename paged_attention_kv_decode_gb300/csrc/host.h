@@ -58,6 +58,12 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 int launch_merge_ex(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,
                     float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int skip_single,
                     cudaStream_t st);
+// The merge of the sequences with two or more partitions only (the others were
+// written directly): one CTA per SM lists them and takes their rows in turn.
+// Falls back to launch_merge_ex(..., skip_single = 1) outside its reach.
+int launch_merge_split_rows(const float* part_out, const float* part_lse, const int32_t* seq_lens, int P, void* out,
+                            float* lse_out, int S, int H, int D, int max_parts, int out_dtype, int sms,
+                            cudaStream_t st);
 
 // The single-token sequences of a chunked-prefill batch through the bf16 decode
 // kernel (decode.cu); rows = the batch's cu_q_lens.  Other sequences are skipped.

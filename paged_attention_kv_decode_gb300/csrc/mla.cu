@@ -1122,7 +1122,7 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
                         "mla_decode_kernel launch", tmKV, tmKVh, p);
   if (rc) return rc;
   if (partition_size > 0 && lay.max_parts > 1)
-    rc = launch_merge_ex(p.part_out, p.part_lse, seq_lens, partition_size, out, lse_out, num_seqs, num_heads, kMlaDv,
-                         lay.max_parts, METIS_BF16, 1, st);
+    rc = launch_merge_split_rows(p.part_out, p.part_lse, seq_lens, partition_size, out, lse_out, num_seqs, num_heads,
+                                 kMlaDv, lay.max_parts, METIS_BF16, sms, st);
   return rc;
 }
