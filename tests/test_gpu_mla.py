@@ -168,3 +168,22 @@ def test_more_items_than_the_schedule_sorts():
     assert_parity(out, ref_o, torch.bfloat16)
     assert_lse(lse, ref_l, torch.bfloat16, exchange_bound(case))
     assert pa.metis_read_status() == 0
+
+
+@pytest.mark.parametrize("num_seqs", [300, 600])
+def test_split_sequences_among_many(num_seqs):
+    """Many short sequences split into 64-token partitions: a mix of empty, one-partition
+    and multi-partition sequences.  Up to 512 sequences the merge lists the split ones
+    itself; above, the work list comes from the schedule kernel and every row goes
+    through the per-row merge."""
+    rng = np.random.default_rng(9 + num_seqs)
+    lens = list(rng.integers(0, 300, num_seqs))
+    lens[0], lens[1] = 0, 64                      # an empty and an exactly one-partition sequence
+    case = wl.make_mla_case(64, lens, H=16, bs=16, poison=True, extra_blocks=2)
+    ref_o, ref_l = oracle.mla_decode(case.q, case.kv_cache, case.block_table, case.seq_lens, case.scale)
+    out, lse = pa.metis_mla_decode(dev(case.q), dev(case.kv_cache), dev(case.block_table), dev(case.seq_lens),
+                                   case.scale, partition_size=64, max_seq_len=case.max_seq_len, want_lse=True)
+    torch.cuda.synchronize()
+    assert_parity(out, ref_o, torch.bfloat16)
+    assert_lse(lse, ref_l, torch.bfloat16, exchange_bound(case))
+    assert pa.metis_read_status() == 0
