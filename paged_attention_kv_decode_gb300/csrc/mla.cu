@@ -132,7 +132,7 @@ struct MlaBar {
                : 1;
   }
 };
-static_assert((MlaBar::kCount + 3) * 8 <= 512, "MLA barrier area");
+static_assert((MlaBar::kCount + 4) * 8 <= 512, "MLA barrier area");
 
 struct MlaParams {
   const uint4* q;   // [S, H, 576] bf16, read as 16-byte chunks
@@ -237,6 +237,16 @@ __device__ __forceinline__ MlaWork mla_work_decode(const MlaParams& p, int4 raw)
   return w;
 }
 
+// A work's cost, for dealing the list out: its units plus the fixed cost of a work
+// boundary, ~5 units (per-cluster finish times on a GB300 fit 1.16 us per unit plus
+// 5.7 us per work).
+constexpr int kMlaWorkOverheadUnits = 5;
+// Scratch (ints) that the in-kernel ranking uses, inside the exchange slots, which
+// are free until the pipelines start.
+constexpr int kMlaScratchInts = 2 * MlaShape::kSlotB / 4;
+constexpr int kMlaDealFixed = 2 * kMlaInlineSeqs + 32 + 2 * kMlaThreads + kMlaWorkCache;
+constexpr int kMlaDealMax = (kMlaScratchInts - kMlaDealFixed) / 2;  // works the dealt list can hold
+
 // Small batches: the works of cluster cl of G, ranked by every CTA itself instead
 // of by a schedule kernel.  The list is every (sequence, partition) ordered by
 // tokens, heaviest first, ties in (sequence, partition) order -- the schedule
@@ -245,15 +255,29 @@ __device__ __forceinline__ MlaWork mla_work_decode(const MlaParams& p, int4 raw)
 // the list is: every full partition in sequence order (a prefix sum), the partial
 // ones by rem (a count over the sequences), every empty one in sequence order (a
 // prefix sum).  Without a split each sequence is one "partial" partition of all
-// its tokens.  Thread t ranks sequence t (S <= the block size); sWorks[r] receives
-// the work at the cluster's r-th snake position.  `scratch` holds kMlaInlineSeqs +
-// 32 ints.  Returns the number of works (items x head tiles); the list has fewer
-// than 2^15 items.
+// its tokens.  Thread t ranks sequence t (S <= the block size).
+//
+// The list is then dealt out in rounds of G positions: round 0 gives position c to
+// cluster c; each later round gives its positions, heaviest first, to the clusters
+// in the order of their cost so far, lightest first (ties: lower cluster index),
+// with the cost of a work its units plus kMlaWorkOverheadUnits -- longest-processing-
+// time-first by rounds.  (A snake over the list, positions c, 2G - 1 - c, 2G + c, ...,
+// balances the units but hands the last partial round's small works to clusters that
+// already hold the heaviest ones.)  Lists longer than kMlaDealMax fall back to the
+// snake.  sWorks[r] receives the cluster's r-th work, *n_mine the number of them
+// (written by thread 0).  Returns the number of works (items x head tiles); the list
+// has fewer than 2^15 items.  `scratch` holds kMlaScratchInts ints.
 __device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_lens, int S, int P, int cap,
                                                int max_parts, int head_tiles, int* scratch, int4* sWorks, int cl,
-                                               int G) {
-  int* sRem = scratch;                      // [S] tokens of the partial partition (0: none)
-  int* sWarp = scratch + kMlaInlineSeqs;    // scan scratch
+                                               int G, int* n_mine) {
+  int* sRem = scratch;                               // [S] tokens of the partial partition (0: none)
+  int* sWarp = sRem + kMlaInlineSeqs;                // scan scratch
+  int* sLen = sWarp + 32;                            // [S] raw lengths
+  int* sLoad = sLen + kMlaInlineSeqs;                // [G] cost dealt to each cluster
+  int* sOrder = sLoad + kMlaThreads;                 // [G] a cluster's place in a round
+  int* sMine = sOrder + kMlaThreads;                 // [rounds] this cluster's list positions
+  int* sCost = sMine + kMlaWorkCache;                // [n_work] cost of each list position
+  int* sWork = sCost + kMlaDealMax;                  // [n_work] sq << 16 | q << 4 | ht of each position
   const int sq = threadIdx.x;
   int np = 0, full = 0, has = 0, rem = 0, Lr = 0;
   if (sq < S) {
@@ -269,6 +293,7 @@ __device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_l
       has = rem > 0;
     }
     sRem[sq] = rem;
+    sLen[sq] = Lr;
   }
   const int empty = np - full - has;
   // full and empty counts packed in one scan (each list total is below 2^15)
@@ -278,9 +303,20 @@ __device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_l
   const int F = tot & 0xffff, E = tot >> 16;
   const int n_work = (F + n_partial + E) * head_tiles;
   if (cl >= n_work) return n_work;
+  const int rounds = (n_work + G - 1) / G;
+  const bool deal = n_work <= kMlaDealMax && G <= kMlaThreads && rounds <= kMlaWorkCache && head_tiles < 16 &&
+                    max_parts < 4096 && S <= 32767;
   int partial_rank = F;
   if (has) {
-    for (int t = 0; t < S; ++t) {
+    int t = 0;
+    for (; t + 8 <= S; t += 8) {  // eight independent shared-memory reads in flight
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int r2 = sRem[t + u];
+        partial_rank += (r2 > rem) || (r2 == rem && t + u < sq);
+      }
+    }
+    for (; t < S; ++t) {
       const int r2 = sRem[t];
       partial_rank += (r2 > rem) || (r2 == rem && t < sq);
     }
@@ -289,12 +325,66 @@ __device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_l
     const int rank = q < full ? (before & 0xffff) + q
                      : (q == full && has) ? partial_rank
                                           : F + n_partial + (before >> 16) + (q - full - has);
+    const int tokens = q < full ? P : (q == full && has) ? rem : 0;
     for (int ht = 0; ht < head_tiles; ++ht) {
       const int pos = rank * head_tiles + ht;
-      const int row = pos / G, col = pos - row * G;
-      if (((row & 1) ? G - 1 - col : col) == cl) sWorks[row] = make_int4(sq, q, ht, Lr);
+      if (deal) {
+        // clamped: a work that heavy is alone on its cluster anyway, and the sums stay in 32 bits
+        sCost[pos] = min((tokens + kMlaUnit - 1) / kMlaUnit, 1 << 20) + kMlaWorkOverheadUnits;
+        sWork[pos] = (sq << 16) | (q << 4) | ht;
+      } else {
+        const int row = pos / G, col = pos - row * G;
+        if (((row & 1) ? G - 1 - col : col) == cl) sWorks[row] = make_int4(sq, q, ht, Lr);
+      }
     }
   }
+  if (!deal) {
+    if (threadIdx.x == 0) {
+      int n = 0;
+      while (mla_work_pos(cl, G, n) < n_work) ++n;
+      *n_mine = n;
+    }
+    return n_work;
+  }
+  __syncthreads();
+  const int c = threadIdx.x;
+  if (c < G) sLoad[c] = c < n_work ? sCost[c] : 0;
+  if (c == 0) sMine[0] = cl;
+  for (int r = 1; r < rounds; ++r) {
+    __syncthreads();
+    if (c < G) {  // place of cluster c in this round: lighter clusters first
+      const int lc = sLoad[c];
+      int order = 0, k = 0;
+      for (; k + 8 <= G; k += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int lk = sLoad[k + u];
+          order += (lk < lc) || (lk == lc && k + u < c);
+        }
+      }
+      for (; k < G; ++k) {
+        const int lk = sLoad[k];
+        order += (lk < lc) || (lk == lc && k < c);
+      }
+      sOrder[c] = order;
+    }
+    __syncthreads();
+    if (c < G) {
+      const int pos = r * G + sOrder[c];
+      if (pos < n_work) sLoad[c] += sCost[pos];
+      if (c == cl) sMine[r] = pos < n_work ? pos : -1;
+    }
+  }
+  __syncthreads();
+  if (c < rounds) {
+    const int pos = sMine[c];
+    if (pos >= 0) {
+      const int wv = sWork[pos], s = wv >> 16;
+      sWorks[c] = make_int4(s, (wv >> 4) & 0xfff, wv & 15, sLen[s]);
+    }
+  }
+  // only the last round can leave a cluster without a position
+  if (c == 0) *n_mine = sMine[rounds - 1] >= 0 ? rounds : rounds - 1;
   return n_work;
 }
 
@@ -338,24 +428,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   // The cluster's works, cached in shared memory (every role walks the same list;
   // the units of all works are numbered g = 0, 1, ...).
   int4* sWorks = reinterpret_cast<int4*>(smem + Sh::kWorks);
-  int* sCount = reinterpret_cast<int*>(bars + MlaBar::kCount + 2);  // [0] units of the cluster, [1] works
+  // [0] units of the cluster, [1] works, [2] works of the cluster (in-kernel list)
+  int* sCount = reinterpret_cast<int*>(bars + MlaBar::kCount + 2);
   if (threadIdx.x == 0) sCount[0] = 0;
-  int n_work;
+  int n_work, n_mine = 0;
   int my_units = 0;
   if (p.inline_list) {
     const int nw = mla_rank_inline(p.seq_lens, p.S, p.P, p.cap, p.max_parts, p.head_tiles,
-                                   reinterpret_cast<int*>(sSlot), sWorks, cl, G);
+                                   reinterpret_cast<int*>(sSlot), sWorks, cl, G, sCount + 2);
     // read back from shared memory: a value the compiler sees as uniform (a
     // per-thread copy would hold a register through every role below)
     if (threadIdx.x == 0) sCount[1] = nw;
     __syncthreads();
     n_work = sCount[1];
     if (cl >= n_work) return;  // both CTAs of the cluster take the same branch
-    __syncthreads();
-    for (int r = threadIdx.x; r < kMlaWorkCache; r += kMlaThreads) {
-      if (mla_work_pos(cl, G, r) >= n_work) break;
-      my_units += mla_work_decode(p, sWorks[r]).n_units;
-    }
+    n_mine = sCount[2];
+    for (int r = threadIdx.x; r < n_mine; r += kMlaThreads) my_units += mla_work_decode(p, sWorks[r]).n_units;
   } else {
     n_work = *p.item_count * p.head_tiles;
     if (cl >= n_work) return;  // both CTAs of the cluster take the same branch
@@ -371,13 +459,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   atomicAdd(sCount, my_units);
   __syncthreads();
   int g_total = sCount[0];
-  for (int r = kMlaWorkCache;; ++r) {  // works past the cache (very long lists only)
-    const long long pos = mla_work_pos(cl, G, r);
-    if (pos >= n_work) break;
-    g_total += mla_work_decode(p, mla_work_raw(p, pos)).n_units;
-  }
+  if (!p.inline_list)
+    for (int r = kMlaWorkCache;; ++r) {  // works past the cache (very long lists only)
+      const long long pos = mla_work_pos(cl, G, r);
+      if (pos >= n_work) break;
+      g_total += mla_work_decode(p, mla_work_raw(p, pos)).n_units;
+    }
   // the cluster's r-th work; false past the end
   auto mla_work = [&](const MlaParams&, int, int, int, int r, MlaWork& w) -> bool {
+    if (p.inline_list) {
+      if (r >= n_mine) return false;
+      w = mla_work_decode(p, sWorks[r]);
+      return true;
+    }
     const long long pos = mla_work_pos(cl, G, r);
     if (pos >= n_work) return false;
     w = mla_work_decode(p, r < kMlaWorkCache ? sWorks[r] : mla_work_raw(p, pos));
