@@ -136,6 +136,7 @@ static_assert((MlaBar::kCount + 4) * 8 <= 512, "MLA barrier area");
 
 struct MlaParams {
   const uint4* q;   // [S, H, 576] bf16, read as 16-byte chunks
+  const void* kv;   // [num_blocks, bs, 576] bf16 (read through the tensor maps; its address for L2 prefetches)
   const int32_t* block_table;
   const int32_t* seq_lens;
   void* out;
@@ -267,9 +268,18 @@ constexpr int kMlaDealMax = (kMlaScratchInts - kMlaDealFixed) / 2;  // works the
 // snake.  sWorks[r] receives the cluster's r-th work, *n_mine the number of them
 // (written by thread 0).  Returns the number of works (items x head tiles); the list
 // has fewer than 2^15 items.  `scratch` holds kMlaScratchInts ints.
-__device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_lens, int S, int P, int cap,
-                                               int max_parts, int head_tiles, int* scratch, int4* sWorks, int cl,
-                                               int G, int* n_mine) {
+// Warm L2 with the 16-byte aligned interior of [ptr, ptr + bytes): one bulk prefetch,
+// no registers, no completion.
+__device__ __forceinline__ void l2_prefetch_bytes(const void* ptr, size_t bytes) {
+  const uintptr_t lo = (reinterpret_cast<uintptr_t>(ptr) + 15) & ~(uintptr_t)15;
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(ptr) + bytes) & ~(uintptr_t)15;
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
+}
+
+__device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch, int4* sWorks, int cl, int G,
+                                               int* n_mine) {
+  const int S = p.S, P = p.P, cap = p.cap, max_parts = p.max_parts, head_tiles = p.head_tiles;
   int* sRem = scratch;                               // [S] tokens of the partial partition (0: none)
   int* sWarp = sRem + kMlaInlineSeqs;                // scan scratch
   int* sLen = sWarp + 32;                            // [S] raw lengths
@@ -281,7 +291,7 @@ __device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_l
   const int sq = threadIdx.x;
   int np = 0, full = 0, has = 0, rem = 0, Lr = 0;
   if (sq < S) {
-    Lr = seq_lens[sq];
+    Lr = p.seq_lens[sq];
     const int Lc = max(0, min(Lr, cap));
     np = mla_parts_of(P, max_parts, Lr);
     if (P <= 0) {
@@ -328,6 +338,20 @@ __device__ __forceinline__ int mla_rank_inline(const int32_t* __restrict__ seq_l
     const int tokens = q < full ? P : (q == full && has) ? rem : 0;
     for (int ht = 0; ht < head_tiles; ++ht) {
       const int pos = rank * head_tiles + ht;
+      if (pos == cl && (blockIdx.x & 1) == 0 && tokens > 0) {
+        // The cluster's first work (round 0): its queries and first pages are cold.
+        // Warming L2 with them while the list is dealt lets the query load and the
+        // ring's first TMA loads, which start after it, read L2.
+        const int rows = min(kMlaRows, p.H - ht * kMlaRows);
+        l2_prefetch_bytes(p.q + ((size_t)sq * p.H + ht * kMlaRows) * (kMlaDq / 8), (size_t)rows * kMlaDq * 2);
+        const int t0 = P > 0 ? q * P : 0, t1 = t0 + min(tokens, kMlaStages * kMlaUnit);
+        for (int pg = t0 / p.bs; pg * p.bs < t1 && pg < p.max_blocks; ++pg) {
+          const int b = p.block_table[(size_t)sq * p.max_blocks + pg];
+          if (b >= 0 && b < p.num_blocks)
+            l2_prefetch_bytes(reinterpret_cast<const char*>(p.kv) + (size_t)b * p.bs * kMlaDq * 2,
+                              (size_t)p.bs * kMlaDq * 2);
+        }
+      }
       if (deal) {
         // clamped: a work that heavy is alone on its cluster anyway, and the sums stay in 32 bits
         sCost[pos] = min((tokens + kMlaUnit - 1) / kMlaUnit, 1 << 20) + kMlaWorkOverheadUnits;
@@ -434,8 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   int n_work, n_mine = 0;
   int my_units = 0;
   if (p.inline_list) {
-    const int nw = mla_rank_inline(p.seq_lens, p.S, p.P, p.cap, p.max_parts, p.head_tiles,
-                                   reinterpret_cast<int*>(sSlot), sWorks, cl, G, sCount + 2);
+    const int nw = mla_rank_inline(p, reinterpret_cast<int*>(sSlot), sWorks, cl, G, sCount + 2);
     // read back from shared memory: a value the compiler sees as uniform (a
     // per-thread copy would hold a register through every role below)
     if (threadIdx.x == 0) sCount[1] = nw;
@@ -1142,6 +1165,7 @@ extern "C" int metis_mla_decode(const void* q, const void* kv_cache, const int32
 
   MlaParams p{};
   p.q = reinterpret_cast<const uint4*>(q);
+  p.kv = kv_cache;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.out = out;
