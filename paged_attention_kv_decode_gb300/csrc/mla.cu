@@ -316,21 +316,30 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
   const int rounds = (n_work + G - 1) / G;
   const bool deal = n_work <= kMlaDealMax && G <= kMlaThreads && rounds <= kMlaWorkCache && head_tiles < 16 &&
                     max_parts < 4096 && S <= 32767;
-  int partial_rank = F;
-  if (has) {
-    int t = 0;
-    for (; t + 8 <= S; t += 8) {  // eight independent shared-memory reads in flight
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int r2 = sRem[t + u];
-        partial_rank += (r2 > rem) || (r2 == rem && t + u < sq);
+  // The rank of each sequence's partial partition: how many partial partitions are
+  // heavier (ties: lower sequence first), counted by `ways` threads per sequence
+  // (consecutive lanes), each over a share of the sequences.
+  int* sPRank = sLoad;  // [S], free until the list is dealt
+  {
+    int ways = 1;
+    while (ways < 8 && S * ways * 2 <= kMlaThreads) ways *= 2;
+    const int s_of = threadIdx.x / ways, part = threadIdx.x & (ways - 1);
+    int cnt = 0, rem_s = 0;
+    const bool live = s_of < S;
+    if (live) rem_s = sRem[s_of];
+    // the sequence has a partial partition: any length when unsplit (P <= 0, the whole
+    // sequence, possibly empty), else a remainder
+    if (live && (P <= 0 || rem_s > 0)) {
+      for (int t = part; t < S; t += ways) {
+        const int r2 = sRem[t];
+        cnt += (r2 > rem_s) || (r2 == rem_s && t < s_of);
       }
     }
-    for (; t < S; ++t) {
-      const int r2 = sRem[t];
-      partial_rank += (r2 > rem) || (r2 == rem && t < sq);
-    }
+    for (int o = ways >> 1; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (live && part == 0) sPRank[s_of] = cnt;
+    __syncthreads();
   }
+  const int partial_rank = F + (has ? sPRank[sq] : 0);
   for (int q = 0; q < np; ++q) {
     const int rank = q < full ? (before & 0xffff) + q
                      : (q == full && has) ? partial_rank
@@ -344,13 +353,21 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
         // ring's first TMA loads, which start after it, read L2.
         const int rows = min(kMlaRows, p.H - ht * kMlaRows);
         l2_prefetch_bytes(p.q + ((size_t)sq * p.H + ht * kMlaRows) * (kMlaDq / 8), (size_t)rows * kMlaDq * 2);
+        // the pages of the ring's first units: their block ids are loaded together (a
+        // load, then its prefetch, one page at a time holds every thread of the CTA at
+        // the next barrier for a memory round trip per page)
+        constexpr int kMaxPages = kMlaStages * kMlaUnit / 16;
         const int t0 = P > 0 ? q * P : 0, t1 = t0 + min(tokens, kMlaStages * kMlaUnit);
-        for (int pg = t0 / p.bs; pg * p.bs < t1 && pg < p.max_blocks; ++pg) {
-          const int b = p.block_table[(size_t)sq * p.max_blocks + pg];
-          if (b >= 0 && b < p.num_blocks)
-            l2_prefetch_bytes(reinterpret_cast<const char*>(p.kv) + (size_t)b * p.bs * kMlaDq * 2,
+        const int pg0 = t0 / p.bs, n_pg = min(min((t1 - 1) / p.bs - pg0 + 1, kMaxPages), p.max_blocks - pg0);
+        int bid[kMaxPages];
+#pragma unroll
+        for (int i = 0; i < kMaxPages; ++i)
+          bid[i] = i < n_pg ? __ldg(p.block_table + (size_t)sq * p.max_blocks + pg0 + i) : -1;
+#pragma unroll
+        for (int i = 0; i < kMaxPages; ++i)
+          if (bid[i] >= 0 && bid[i] < p.num_blocks)
+            l2_prefetch_bytes(reinterpret_cast<const char*>(p.kv) + (size_t)bid[i] * p.bs * kMlaDq * 2,
                               (size_t)p.bs * kMlaDq * 2);
-        }
       }
       if (deal) {
         // clamped: a work that heavy is alone on its cluster anyway, and the sums stay in 32 bits
@@ -479,7 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       my_units += mla_work_decode(p, raw).n_units;
     }
   }
-  atomicAdd(sCount, my_units);
+  if (my_units) atomicAdd(sCount, my_units);
   __syncthreads();
   int g_total = sCount[0];
   if (!p.inline_list)
