@@ -258,12 +258,12 @@ constexpr int kMlaDealMax = (kMlaScratchInts - kMlaDealFixed) / 2;  // works the
 // prefix sum).  Without a split each sequence is one "partial" partition of all
 // its tokens.  Thread t ranks sequence t (S <= the block size).
 //
-// The list is then dealt out in rounds of G positions: round 0 gives position c to
-// cluster c; each later round gives its positions, heaviest first, to the clusters
+// The list is then dealt out in passes of G positions: pass 0 gives position c to
+// cluster c; each later pass gives its positions, heaviest first, to the clusters
 // in the order of their cost so far, lightest first (ties: lower cluster index),
 // with the cost of a work its units plus kMlaWorkOverheadUnits -- longest-processing-
-// time-first by rounds.  (A snake over the list, positions c, 2G - 1 - c, 2G + c, ...,
-// balances the units but hands the last partial round's small works to clusters that
+// time-first by passes.  (A snake over the list, positions c, 2G - 1 - c, 2G + c, ...,
+// balances the units but hands the last partial pass's small works to clusters that
 // already hold the heaviest ones.)  Lists longer than kMlaDealMax fall back to the
 // snake.  sWorks[r] receives the cluster's r-th work, *n_mine the number of them
 // (written by thread 0).  Returns the number of works (items x head tiles); the list
@@ -284,8 +284,8 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
   int* sWarp = sRem + kMlaInlineSeqs;                // scan scratch
   int* sLen = sWarp + 32;                            // [S] raw lengths
   int* sLoad = sLen + kMlaInlineSeqs;                // [G] cost dealt to each cluster
-  int* sOrder = sLoad + kMlaThreads;                 // [G] a cluster's place in a round
-  int* sMine = sOrder + kMlaThreads;                 // [rounds] this cluster's list positions
+  int* sOrder = sLoad + kMlaThreads;                 // [G] a cluster's place in a pass
+  int* sMine = sOrder + kMlaThreads;                 // [passes] this cluster's list positions
   int* sCost = sMine + kMlaWorkCache;                // [n_work] cost of each list position
   int* sWork = sCost + kMlaDealMax;                  // [n_work] sq << 16 | q << 4 | ht of each position
   const int sq = threadIdx.x;
@@ -313,8 +313,8 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
   const int F = tot & 0xffff, E = tot >> 16;
   const int n_work = (F + n_partial + E) * head_tiles;
   if (cl >= n_work) return n_work;
-  const int rounds = (n_work + G - 1) / G;
-  const bool deal = n_work <= kMlaDealMax && G <= kMlaThreads && rounds <= kMlaWorkCache && head_tiles < 16 &&
+  const int passes = (n_work + G - 1) / G;
+  const bool deal = n_work <= kMlaDealMax && G <= kMlaThreads && passes <= kMlaWorkCache && head_tiles < 16 &&
                     max_parts < 4096 && S <= 32767;
   // The rank of each sequence's partial partition: how many partial partitions are
   // heavier (ties: lower sequence first), counted by `ways` threads per sequence
@@ -348,7 +348,7 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
     for (int ht = 0; ht < head_tiles; ++ht) {
       const int pos = rank * head_tiles + ht;
       if (pos == cl && (blockIdx.x & 1) == 0 && tokens > 0) {
-        // The cluster's first work (round 0): its queries and first pages are cold.
+        // The cluster's first work (pass 0): its queries and first pages are cold.
         // Warming L2 with them while the list is dealt lets the query load and the
         // ring's first TMA loads, which start after it, read L2.
         const int rows = min(kMlaRows, p.H - ht * kMlaRows);
@@ -391,9 +391,9 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
   const int c = threadIdx.x;
   if (c < G) sLoad[c] = c < n_work ? sCost[c] : 0;
   if (c == 0) sMine[0] = cl;
-  for (int r = 1; r < rounds; ++r) {
+  for (int r = 1; r < passes; ++r) {
     __syncthreads();
-    if (c < G) {  // place of cluster c in this round: lighter clusters first
+    if (c < G) {  // place of cluster c in this pass: lighter clusters first
       const int lc = sLoad[c];
       int order = 0, k = 0;
       for (; k + 8 <= G; k += 8) {
@@ -417,15 +417,15 @@ __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch,
     }
   }
   __syncthreads();
-  if (c < rounds) {
+  if (c < passes) {
     const int pos = sMine[c];
     if (pos >= 0) {
       const int wv = sWork[pos], s = wv >> 16;
       sWorks[c] = make_int4(s, (wv >> 4) & 0xfff, wv & 15, sLen[s]);
     }
   }
-  // only the last round can leave a cluster without a position
-  if (c == 0) *n_mine = sMine[rounds - 1] >= 0 ? rounds : rounds - 1;
+  // only the last pass can leave a cluster without a position
+  if (c == 0) *n_mine = sMine[passes - 1] >= 0 ? passes : passes - 1;
   return n_work;
 }
 
@@ -567,7 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool row_valid;
     const uint4* src = q_row(w, hr, row_valid);
-    for (int c0 = 0; c0 < 128; c0 += 64) {  // two rounds of 256 B of the row's latent half (rope last)
+    for (int c0 = 0; c0 < 128; c0 += 64) {  // two passes of 256 B of the row's latent half (rope last)
       uint32_t v[64];
       if (p.q_v8) {
 #pragma unroll
