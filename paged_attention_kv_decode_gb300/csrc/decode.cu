@@ -21,7 +21,14 @@
 //                       Warps merge their (m, l, O) states in shared memory.
 //   decode_f32_kernel   fp32 K/V on FMA units (the 1e-5 path): each warp
 //                       walks tokens, lanes split head_dim.
-//   merge_kernel        one CTA per (sequence, head): the log-sum-exp merge.
+//   merge_kernel        one CTA per (sequence, head): the log-sum-exp merge of
+//                       many partitions.
+//   merge_warp_kernel   one warp per (sequence, head): the merge of at most 16.
+//   merge_split_rows_kernel  the rows of the sequences with two or more
+//                       partitions only, one CTA per SM (MLA's merge).
+//   decode_rows_beside_kernel  the single-token sequences of a chunked-prefill
+//                       batch, persistent, on the SMs the chunk kernel leaves
+//                       them.
 #include <math.h>
 
 #include <algorithm>
