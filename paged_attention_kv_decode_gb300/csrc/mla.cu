@@ -238,6 +238,15 @@ __device__ __forceinline__ MlaWork mla_work_decode(const MlaParams& p, int4 raw)
   return w;
 }
 
+// Warm L2 with the 16-byte aligned interior of [ptr, ptr + bytes): one bulk prefetch,
+// no registers, no completion.
+__device__ __forceinline__ void l2_prefetch_bytes(const void* ptr, size_t bytes) {
+  const uintptr_t lo = (reinterpret_cast<uintptr_t>(ptr) + 15) & ~(uintptr_t)15;
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(ptr) + bytes) & ~(uintptr_t)15;
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
+}
+
 // A work's cost, for dealing the list out: its units plus the fixed cost of a work
 // boundary, ~5 units (per-cluster finish times on a GB300 fit 1.16 us per unit plus
 // 5.7 us per work).
@@ -266,17 +275,10 @@ constexpr int kMlaDealMax = (kMlaScratchInts - kMlaDealFixed) / 2;  // works the
 // balances the units but hands the last partial pass's small works to clusters that
 // already hold the heaviest ones.)  Lists longer than kMlaDealMax fall back to the
 // snake.  sWorks[r] receives the cluster's r-th work, *n_mine the number of them
-// (written by thread 0).  Returns the number of works (items x head tiles); the list
-// has fewer than 2^15 items.  `scratch` holds kMlaScratchInts ints.
-// Warm L2 with the 16-byte aligned interior of [ptr, ptr + bytes): one bulk prefetch,
-// no registers, no completion.
-__device__ __forceinline__ void l2_prefetch_bytes(const void* ptr, size_t bytes) {
-  const uintptr_t lo = (reinterpret_cast<uintptr_t>(ptr) + 15) & ~(uintptr_t)15;
-  const uintptr_t hi = (reinterpret_cast<uintptr_t>(ptr) + bytes) & ~(uintptr_t)15;
-  if (hi > lo)
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
-}
-
+// (written by thread 0).  On the way, the thread that ranks the cluster's pass-0 work
+// warms L2 with that work's queries and first pages (rank-0 CTA only).  Returns the
+// number of works (items x head tiles); the list has fewer than 2^15 items.
+// `scratch` holds kMlaScratchInts ints.
 __device__ __forceinline__ int mla_rank_inline(const MlaParams& p, int* scratch, int4* sWorks, int cl, int G,
                                                int* n_mine) {
   const int S = p.S, P = p.P, cap = p.cap, max_parts = p.max_parts, head_tiles = p.head_tiles;
