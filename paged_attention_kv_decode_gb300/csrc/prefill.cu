@@ -176,7 +176,8 @@ constexpr int kSchedThreads = 1024;
 // a 3-stage ring: ~192 KB in flight; timestamps on a GB300 show 453 MB of decodes
 // taking ~253 us on 24 SMs beside 16 chunks of 512, i.e. ~75 GB/s per SM.  Too few
 // decode SMs, so that the decodes finish last, costs far more than a few too many),
-// and the chunk kernel's FLOP/s (the chunks alone reach ~1.07 PFLOP/s on 152 SMs).
+// and the chunk kernel's FLOP/s (the chunks alone reach ~1.07-1.13 PFLOP/s on 152 SMs;
+// with 7 TFLOP/s per SM the mixed batch above ends its decodes and chunks together).
 constexpr float kDecSmBytesPerS = 75e9f;
 constexpr float kChunkSmFlopsPerS = 7.0e12f;
 
